@@ -1,0 +1,385 @@
+/*
+ * kda_oracle.c -- plain, slow, fp64 CPU oracle for the Kimi Delta Attention
+ * (KDA) forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link or
+ * call this file: only the test-suite, the smoke check and the CPU-baseline leg
+ * of the benchmark use it.  It shares no code, header, table or helper with
+ * the CUDA library.
+ *
+ * What it computes
+ * ----------------
+ * "Flashkda Delta Attention", section "Core Kernel API", gives the call
+ *   fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+ *       initial_state=None, final_state=None, cu_seqlens=None)
+ * and says the kernel performs the recurrent state updates of delta attention.
+ * "MoonshotAI/FlashKDA" (trend summary), section "Kernel API and Constraints",
+ * fixes K = V = 128, allows cu_seqlens only with B = 1 and lets each state be
+ * bf16, fp32 or absent.  The pages print no formula, so this oracle takes the
+ * plain reading of a gated delta rule with a per-channel (per key-dimension)
+ * decay, run independently for every sequence n and head h:
+ *
+ *   x_t      = g_t + dt_bias[h]                       (vector over K channels)
+ *   la_t     = max(-exp(A_log[h]) * softplus(x_t), lower_bound)   (log decay)
+ *   S        <- Diag(exp(la_t)) S                     (S is K x V, S[c][j])
+ *   S        <- S + beta_t k_t (v_t - S^T k_t)^T      (delta-rule write)
+ *   o_t      = scale * S^T q_t
+ *
+ * which is S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T.
+ * The gate form (softplus of g + dt_bias, scaled by -exp(A_log), clamped
+ * below at lower_bound) is a reading: the pages only name A_log, dt_bias and
+ * lower_bound in the argument list.  softplus is evaluated exactly as
+ * max(x,0) + log1p(exp(-|x|)) (no threshold shortcut).
+ *
+ * Two forms are provided:
+ *   kda_oracle_fwd_*   the token-by-token recurrence above (the definition);
+ *   kda_oracle_chunk   one chunk of the chunkwise form (cumsum G, strictly
+ *                      lower A, T = (I + A)^-1 by forward substitution, WY
+ *                      factors W and U, the query/key score matrix and the
+ *                      chunk-end decay), with every exponential taken
+ *                      elementwise on a difference of cumulative sums, and
+ *   kda_oracle_fwd_chunked, which chains kda_oracle_chunk over a sequence.
+ * The chunked form exists so that the test-suite can check it against the
+ * recurrence and expose per-chunk intermediates; it is not used to define
+ * anything.
+ *
+ * Layouts (all row-major, contiguous):
+ *   q, k, g      [NT, H, K]      NT = total tokens (B*T, or the packed length)
+ *   v, out       [NT, H, V]
+ *   beta         [NT, H]
+ *   A_log        [H]             dt_bias [H, K]
+ *   h0, hT       [N, H, K, V]    state S[c][j] = S[(n*H + h)*K*V + c*V + j]
+ *   cu           [N + 1]         token offsets of the N sequences
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+#define ORACLE_ENOMEM 2
+
+int kda_oracle_abi_version(void) { return 1; }
+
+/* bf16 bit pattern -> exact double (bf16 is the top half of an IEEE fp32). */
+static double bf16_bits_to_double(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double softplus(double x) {
+    double pos = x > 0.0 ? x : 0.0;
+    return pos + log1p(exp(-fabs(x)));
+}
+
+/* Log-decay of one channel (see header). */
+double kda_oracle_log_decay(double g, double A_log, double dt_bias, double lower_bound) {
+    double la = -exp(A_log) * softplus(g + dt_bias);
+    return la < lower_bound ? lower_bound : la;
+}
+
+/* Element accessors: the fp64 entry point reads doubles, the "typed" entry
+ * point reads bf16 activations and fp32 / bf16 states and upcasts exactly. */
+typedef struct {
+    int kind; /* 0 = double, 1 = bf16 bits, 2 = float */
+    const void* p;
+} src_t;
+
+static double src_get(src_t s, int64_t i) {
+    switch (s.kind) {
+        case 0: return ((const double*)s.p)[i];
+        case 1: return bf16_bits_to_double(((const uint16_t*)s.p)[i]);
+        default: return (double)((const float*)s.p)[i];
+    }
+}
+
+typedef struct {
+    src_t q, k, v, g, beta, A_log, dt_bias, h0;
+    double scale, lower_bound, erase;
+    double* out;
+    double* hT;
+    const int64_t* cu;
+    int64_t N, H, K, V;
+} problem_t;
+
+static int validate(const problem_t* P) {
+    if (P->N < 0 || P->H <= 0 || P->K <= 0 || P->V <= 0) return ORACLE_EINVAL;
+    if (!P->cu || P->cu[0] != 0) return ORACLE_EINVAL;
+    for (int64_t n = 0; n < P->N; ++n)
+        if (P->cu[n + 1] < P->cu[n]) return ORACLE_EINVAL;
+    return ORACLE_OK;
+}
+
+/* The token-by-token recurrence for one (sequence, head).  S, r and a are
+ * caller-provided scratch of K*V, V and K doubles. */
+static void recur_one(const problem_t* P, int64_t n, int64_t h, double* S, double* r, double* a) {
+    const int64_t K = P->K, V = P->V, H = P->H;
+    const int64_t sbase = (n * H + h) * K * V;
+    for (int64_t i = 0; i < K * V; ++i) S[i] = P->h0.p ? src_get(P->h0, sbase + i) : 0.0;
+    const double A_log = src_get(P->A_log, h);
+    for (int64_t t = P->cu[n]; t < P->cu[n + 1]; ++t) {
+        const int64_t qk_row = (t * H + h) * K;
+        const int64_t v_row = (t * H + h) * V;
+        /* decay */
+        for (int64_t c = 0; c < K; ++c) {
+            double la = kda_oracle_log_decay(src_get(P->g, qk_row + c), A_log,
+                                             src_get(P->dt_bias, h * K + c), P->lower_bound);
+            a[c] = exp(la);
+        }
+        for (int64_t c = 0; c < K; ++c)
+            for (int64_t j = 0; j < V; ++j) S[c * V + j] *= a[c];
+        /* r = S^T k */
+        for (int64_t j = 0; j < V; ++j) r[j] = 0.0;
+        for (int64_t c = 0; c < K; ++c) {
+            const double kc = src_get(P->k, qk_row + c);
+            for (int64_t j = 0; j < V; ++j) r[j] += S[c * V + j] * kc;
+        }
+        /* S += beta k (v - erase * r)^T */
+        const double b = src_get(P->beta, t * H + h);
+        for (int64_t j = 0; j < V; ++j) r[j] = b * (src_get(P->v, v_row + j) - P->erase * r[j]);
+        for (int64_t c = 0; c < K; ++c) {
+            const double kc = src_get(P->k, qk_row + c);
+            for (int64_t j = 0; j < V; ++j) S[c * V + j] += kc * r[j];
+        }
+        /* o = scale S^T q */
+        double* o = P->out + v_row;
+        for (int64_t j = 0; j < V; ++j) o[j] = 0.0;
+        for (int64_t c = 0; c < K; ++c) {
+            const double qc = src_get(P->q, qk_row + c);
+            for (int64_t j = 0; j < V; ++j) o[j] += S[c * V + j] * qc;
+        }
+        for (int64_t j = 0; j < V; ++j) o[j] *= P->scale;
+    }
+    if (P->hT)
+        for (int64_t i = 0; i < K * V; ++i) P->hT[sbase + i] = S[i];
+}
+
+static int run_recurrent(const problem_t* P, int nthreads) {
+    int rc = validate(P);
+    if (rc) return rc;
+    const int64_t pairs = P->N * P->H;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+#endif
+    for (int64_t p = 0; p < pairs; ++p) {
+        double* S = (double*)malloc(sizeof(double) * (size_t)(P->K * P->V + P->V + P->K));
+        if (!S) {
+            failed = 1;
+            continue;
+        }
+        recur_one(P, p / P->H, p % P->H, S, S + P->K * P->V, S + P->K * P->V + P->V);
+        free(S);
+    }
+    return failed ? ORACLE_ENOMEM : ORACLE_OK;
+}
+
+/*
+ * All-fp64 entry point.  erase scales the S^T k term of the delta-rule write
+ * (1 for KDA; 0 gives a plain gated linear-attention write, used only by the
+ * test-suite).  h0 / hT may be NULL.  Returns 0 on success.
+ */
+int kda_oracle_fwd_f64(const double* q, const double* k, const double* v, const double* g,
+                       const double* beta, double scale, const double* A_log,
+                       const double* dt_bias, double lower_bound, const double* h0,
+                       double* out, double* hT, const int64_t* cu, int64_t N, int64_t H,
+                       int64_t K, int64_t V, double erase, int nthreads) {
+    problem_t P = {{0, q}, {0, k}, {0, v}, {0, g}, {0, beta}, {0, A_log}, {0, dt_bias}, {0, h0},
+                   scale, lower_bound, erase, out, hT, cu, N, H, K, V};
+    return run_recurrent(&P, nthreads);
+}
+
+/*
+ * Typed entry point: q, k, v, g, beta are bf16 bit patterns; A_log and
+ * dt_bias are fp32; h0 is fp32 (h0_kind = 2), bf16 (h0_kind = 1) or absent
+ * (h0 = NULL).  Every value is upcast exactly to fp64 before use.
+ */
+int kda_oracle_fwd_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const uint16_t* g, const uint16_t* beta, double scale,
+                        const float* A_log, const float* dt_bias, double lower_bound,
+                        const void* h0, int h0_kind, double* out, double* hT,
+                        const int64_t* cu, int64_t N, int64_t H, int64_t K, int64_t V,
+                        int nthreads) {
+    if (h0 && h0_kind != 1 && h0_kind != 2) return ORACLE_EINVAL;
+    problem_t P = {{1, q}, {1, k}, {1, v}, {1, g}, {1, beta}, {2, A_log}, {2, dt_bias},
+                   {h0 ? h0_kind : 2, h0}, scale, lower_bound, 1.0, out, hT, cu, N, H, K, V};
+    return run_recurrent(&P, nthreads);
+}
+
+/*
+ * One chunk of the chunkwise form, for one head, in fp64.
+ *
+ * Inputs are the chunk's c token rows: q, k (row stride ldk), v (row stride
+ * ldv), per-channel log decays la (c x K, contiguous) and beta (stride ldb).
+ * Outputs (contiguous, any may be NULL):
+ *   G     c x K   G_t = sum_{s<=t} la_s                    (in-chunk cumsum)
+ *   A     c x c   A[i][j] = beta_i sum_ch k_i k_j exp(G_i - G_j), j < i, else 0
+ *   Aqk   c x c   Aqk[i][j] = sum_ch q_i k_j exp(G_i - G_j),      j <= i, else 0
+ *   T     c x c   (I + A)^-1, unit lower triangular, by forward substitution
+ *   W     c x K   T diag(beta) (K o exp(G))
+ *   U     c x V   T diag(beta) V
+ *   gam   K       exp(G_{c-1})                              (chunk-end decay)
+ * With these, for the state S0 entering the chunk,
+ *   Delta = U - W S0,
+ *   o_i   = scale (S0^T (q_i o exp(G_i)) + sum_{j<=i} Aqk[i][j] Delta_j),
+ *   S_end = Diag(gam) S0 + sum_j (k_j o exp(G_{c-1} - G_j)) Delta_j^T,
+ * which follows from unrolling the recurrence across the chunk.
+ */
+int kda_oracle_chunk(const double* q, int64_t ldq, const double* k, int64_t ldk,
+                     const double* v, int64_t ldv, const double* la, const double* beta,
+                     int64_t ldb, int64_t c, int64_t K, int64_t V, double* G, double* A,
+                     double* Aqk, double* T, double* W, double* U, double* gam) {
+    if (c <= 0 || K <= 0 || V <= 0) return ORACLE_EINVAL;
+    double* Gl = (double*)malloc(sizeof(double) * (size_t)(c * K + 3 * c * c));
+    if (!Gl) return ORACLE_ENOMEM;
+    double* Al = Gl + c * K;
+    double* Ql = Al + c * c;
+    double* Tl = Ql + c * c;
+    for (int64_t ch = 0; ch < K; ++ch) {
+        double run = 0.0;
+        for (int64_t t = 0; t < c; ++t) {
+            run += la[t * K + ch];
+            Gl[t * K + ch] = run;
+        }
+    }
+    for (int64_t i = 0; i < c; ++i)
+        for (int64_t j = 0; j < c; ++j) {
+            double skk = 0.0, sqk = 0.0;
+            if (j <= i)
+                for (int64_t ch = 0; ch < K; ++ch) {
+                    const double d = exp(Gl[i * K + ch] - Gl[j * K + ch]);
+                    skk += k[i * ldk + ch] * k[j * ldk + ch] * d;
+                    sqk += q[i * ldq + ch] * k[j * ldk + ch] * d;
+                }
+            Al[i * c + j] = (j < i) ? beta[i * ldb] * skk : 0.0;
+            Ql[i * c + j] = (j <= i) ? sqk : 0.0;
+        }
+    /* forward substitution: row i of T solves (I + A) T = I */
+    for (int64_t i = 0; i < c; ++i)
+        for (int64_t j = 0; j < c; ++j) {
+            double s = (i == j) ? 1.0 : 0.0;
+            for (int64_t l = 0; l < i; ++l) s -= Al[i * c + l] * Tl[l * c + j];
+            Tl[i * c + j] = s;
+        }
+    if (G) memcpy(G, Gl, sizeof(double) * (size_t)(c * K));
+    if (A) memcpy(A, Al, sizeof(double) * (size_t)(c * c));
+    if (Aqk) memcpy(Aqk, Ql, sizeof(double) * (size_t)(c * c));
+    if (T) memcpy(T, Tl, sizeof(double) * (size_t)(c * c));
+    if (W)
+        for (int64_t i = 0; i < c; ++i)
+            for (int64_t ch = 0; ch < K; ++ch) {
+                double s = 0.0;
+                for (int64_t l = 0; l < c; ++l)
+                    s += Tl[i * c + l] * beta[l * ldb] * k[l * ldk + ch] * exp(Gl[l * K + ch]);
+                W[i * K + ch] = s;
+            }
+    if (U)
+        for (int64_t i = 0; i < c; ++i)
+            for (int64_t j = 0; j < V; ++j) {
+                double s = 0.0;
+                for (int64_t l = 0; l < c; ++l) s += Tl[i * c + l] * beta[l * ldb] * v[l * ldv + j];
+                U[i * V + j] = s;
+            }
+    if (gam)
+        for (int64_t ch = 0; ch < K; ++ch) gam[ch] = exp(Gl[(c - 1) * K + ch]);
+    free(Gl);
+    return ORACLE_OK;
+}
+
+/*
+ * The chunkwise form chained over every sequence and head, chunk size C
+ * (chunks start at each sequence start; the last one may be shorter).
+ * Same arguments and layouts as kda_oracle_fwd_f64 (erase is fixed to 1).
+ */
+int kda_oracle_fwd_chunked(const double* q, const double* k, const double* v,
+                           const double* g, const double* beta, double scale,
+                           const double* A_log, const double* dt_bias, double lower_bound,
+                           const double* h0, double* out, double* hT, const int64_t* cu,
+                           int64_t N, int64_t H, int64_t K, int64_t V, int64_t C) {
+    if (C <= 0 || N < 0 || H <= 0 || K <= 0 || V <= 0 || !cu || cu[0] != 0) return ORACLE_EINVAL;
+    for (int64_t n = 0; n < N; ++n)
+        if (cu[n + 1] < cu[n]) return ORACLE_EINVAL;
+    const size_t need = (size_t)(K * V + C * K * 3 + C * C * 3 + C * V * 2 + K);
+    double* buf = (double*)malloc(sizeof(double) * need);
+    if (!buf) return ORACLE_ENOMEM;
+    double* S = buf;
+    double* la = S + K * V;
+    double* G = la + C * K;
+    double* W = G + C * K;
+    double* A = W + C * K;
+    double* Aqk = A + C * C;
+    double* T = Aqk + C * C;
+    double* U = T + C * C;
+    double* D = U + C * V;
+    double* gam = D + C * V;
+    int rc = ORACLE_OK;
+    for (int64_t n = 0; n < N && rc == ORACLE_OK; ++n)
+        for (int64_t h = 0; h < H && rc == ORACLE_OK; ++h) {
+            const int64_t sbase = (n * H + h) * K * V;
+            for (int64_t i = 0; i < K * V; ++i) S[i] = h0 ? h0[sbase + i] : 0.0;
+            for (int64_t t0 = cu[n]; t0 < cu[n + 1]; t0 += C) {
+                const int64_t c = (cu[n + 1] - t0 < C) ? cu[n + 1] - t0 : C;
+                for (int64_t t = 0; t < c; ++t)
+                    for (int64_t ch = 0; ch < K; ++ch)
+                        la[t * K + ch] = kda_oracle_log_decay(g[((t0 + t) * H + h) * K + ch],
+                                                              A_log[h], dt_bias[h * K + ch],
+                                                              lower_bound);
+                const double* qc = q + (t0 * H + h) * K;
+                const double* kc = k + (t0 * H + h) * K;
+                const double* vc = v + (t0 * H + h) * V;
+                const double* bc = beta + t0 * H + h;
+                rc = kda_oracle_chunk(qc, H * K, kc, H * K, vc, H * V, la, bc, H, c, K, V, G, A,
+                                      Aqk, T, W, U, gam);
+                if (rc) break;
+                /* Delta = U - W S0 */
+                for (int64_t i = 0; i < c; ++i)
+                    for (int64_t j = 0; j < V; ++j) {
+                        double s = U[i * V + j];
+                        for (int64_t ch = 0; ch < K; ++ch) s -= W[i * K + ch] * S[ch * V + j];
+                        D[i * V + j] = s;
+                    }
+                /* outputs */
+                for (int64_t i = 0; i < c; ++i)
+                    for (int64_t j = 0; j < V; ++j) {
+                        double s = 0.0;
+                        for (int64_t ch = 0; ch < K; ++ch)
+                            s += qc[i * H * K + ch] * exp(G[i * K + ch]) * S[ch * V + j];
+                        for (int64_t l = 0; l <= i; ++l) s += Aqk[i * c + l] * D[l * V + j];
+                        out[((t0 + i) * H + h) * V + j] = scale * s;
+                    }
+                /* state to the end of the chunk */
+                for (int64_t ch = 0; ch < K; ++ch)
+                    for (int64_t j = 0; j < V; ++j) {
+                        double s = gam[ch] * S[ch * V + j];
+                        for (int64_t l = 0; l < c; ++l)
+                            s += kc[l * H * K + ch] * exp(G[(c - 1) * K + ch] - G[l * K + ch]) *
+                                 D[l * V + j];
+                        S[ch * V + j] = s;
+                    }
+            }
+            if (hT)
+                for (int64_t i = 0; i < K * V; ++i) hT[sbase + i] = S[i];
+        }
+    free(buf);
+    return rc;
+}
+
+/* Log-decays for a block of tokens: la[t][h][c] for g laid out [n_tok, H, K]. */
+int kda_oracle_gate(const double* g, int64_t n_tok, int64_t H, int64_t K, const double* A_log,
+                    const double* dt_bias, double lower_bound, double* la) {
+    if (n_tok < 0 || H <= 0 || K <= 0) return ORACLE_EINVAL;
+    for (int64_t t = 0; t < n_tok; ++t)
+        for (int64_t h = 0; h < H; ++h)
+            for (int64_t c = 0; c < K; ++c) {
+                const int64_t i = (t * H + h) * K + c;
+                la[i] = kda_oracle_log_decay(g[i], A_log[h], dt_bias[h * K + c], lower_bound);
+            }
+    return ORACLE_OK;
+}
