@@ -1,0 +1,376 @@
+#!/usr/bin/env python
+"""KDA forward benchmark on GB300.
+
+Default workload: long_context (B=1, T=65536, H=32, K=V=128, fp32 initial and
+final state, seed 3) -- the configuration the headline metric is quoted on.
+A step is one full forward pass (chunk schedule, chunk kernel, recurrence
+kernel) over that workload with inputs resident in HBM; inputs (2.7 GB per
+step) are far larger than L2 (129 MB), so no explicit flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun, one process per GPU; each rank runs an
+independent replica of the workload (the pass has no cross-GPU exchange), so
+scaling is weak and value = all ranks' head-tokens / max-over-ranks time.
+``--impl reference`` times the fp64 CPU oracle (the reference arm: there is
+no runnable reference implementation) on a bounded sample of the workload.
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA fwd head-tokens/s at T=65536,H=32; % of roofline (bf16 TC vs HBM)"
+UNIT = "head-tokens/s"
+D = 128
+BYTES_PER_HEAD_TOKEN = 4 * 2 * D + 2 + 2 * D   # q, k, v, g reads + beta + out write = 1282
+
+
+# ----------------------------------------------------------------------------- counted work
+
+def seq_lengths(p):
+    if p["cu_seqlens"] is None:
+        return [p["T"]] * p["B"]
+    cu = p["cu_seqlens"].tolist()
+    return [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+
+
+def chunk_flops(c):
+    """Counted FLOPs of one chunk of length c for one head (5c^2D + 6cD^2 + c^3/3)."""
+    return 5 * c * c * D + 6 * c * D * D + c ** 3 / 3.0
+
+
+def counted_work(p):
+    H = p["H"]
+    flops = 0.0
+    for L in seq_lengths(p):
+        full, rem = divmod(L, 64)
+        flops += full * chunk_flops(64) + (chunk_flops(rem) if rem else 0.0)
+    flops *= H
+    head_tokens = p["B"] * p["T"] * H
+    state_bytes = 0
+    sd = p["state_dtype"]
+    if sd is not None:
+        es = 4 if str(sd) == "torch.float32" else 2
+        state_bytes = 2 * p["N"] * H * D * D * es   # read initial + write final
+    return head_tokens, flops, head_tokens * BYTES_PER_HEAD_TOKEN + state_bytes
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_sample(p, target_s, max_tokens=None, fixed=None):
+    """Time the fp64 oracle (as it stands) on the first S tokens of every head."""
+    import torch
+
+    import oracle
+    oracle.build()
+    T = p["T"] if p["cu_seqlens"] is None else int(p["cu_seqlens"][-1])
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    H = p["H"]
+
+    def run(S):
+        # a prefix of the packed token stream, cut into whole sequences
+        if p["cu_seqlens"] is not None:
+            cu = p["cu_seqlens"].tolist()
+            n = max(1, max(i for i in range(len(cu)) if cu[i] <= S))
+            S = cu[n]
+            cu_s = torch.tensor(cu[:n + 1], dtype=torch.int32)
+            h0 = None if p["initial_state"] is None else p["initial_state"][:n]
+        else:
+            cu_s = None
+            h0 = None if p["initial_state"] is None else p["initial_state"][:1]
+        sl = [x[:1, :S].contiguous() for x in (p["q"], p["k"], p["v"], p["g"], p["beta"])]
+        t0 = time.perf_counter()
+        oracle.recurrent(*sl, p["scale"], p["A_log"], p["dt_bias"], p["lower_bound"],
+                         initial_state=h0, cu_seqlens=cu_s, nthreads=cores)
+        return time.perf_counter() - t0, S * H
+
+    if fixed is not None:
+        S = fixed
+        dt, ht = run(S)
+    else:
+        S = min(T, 512)
+        dt, ht = run(S)
+        S2 = int(min(T, max_tokens or T, S * max(1.0, target_s / max(dt, 1e-3))))
+        if S2 > S:
+            dt, ht = run(S2)
+            S = S2
+    pairs = H * (1 if p["cu_seqlens"] is None else
+                 max(1, sum(1 for c in p["cu_seqlens"].tolist()[1:] if c <= S)))
+    threads = min(cores, pairs)
+    return {"value": ht / dt, "unit": UNIT, "cores": threads, "kind": "oracle", "tokens": S,
+            "sample": f"first {S} tokens x {H} heads of the workload ({ht} head-tokens), "
+                      f"fp64 C oracle, OpenMP over (sequence, head), {dt:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long_context")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from gated_delta_rule_30_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        p = inputs.make(w)
+        # each step: the oracle on a fixed bounded sample (first tokens of every head)
+        res = oracle_sample(p, target_s=2.0, max_tokens=2048)
+        S_tokens = res["tokens"]
+        rates = []
+        for i in range(warmup + args.steps):
+            r = oracle_sample(p, target_s=0.0, max_tokens=S_tokens, fixed=S_tokens)
+            if i >= warmup:
+                rates.append(r["value"])
+        val = statistics.median(rates)
+        res = r
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1,
+                "steps": args.steps, "warmup": warmup, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name},
+                "cpu_baseline": {"value": val, "unit": UNIT, "cores": res["cores"],
+                                 "kind": "oracle", "sample": res["sample"]},
+                "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    import torch.distributed as dist
+
+    import gated_delta_rule_30_gb300 as kda
+    from gated_delta_rule_30_gb300 import build as kbuild
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    kbuild.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+
+    p = inputs.make(w)
+    head_tokens, flops, alg_bytes = counted_work(p)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+    out = torch.empty_like(d["v"])
+    hT = None if d["initial_state"] is None else torch.empty_like(d["initial_state"])
+    ws = torch.empty(kda.workspace_size(p["B"], p["T"], p["H"], p["N"] if p["cu_seqlens"] is not None
+                                        else 0, p["cu_seqlens"] is not None),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], out, d["A_log"],
+                d["dt_bias"], d["lower_bound"], initial_state=d["initial_state"], final_state=hT,
+                cu_seqlens=d["cu_seqlens"], workspace=ws)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    kda.device_status(dev)
+
+    # stage events: per-kernel durations measured on the launch stream
+    n_ev = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(dev.index if world == 1 else local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        kda.set_stage_events(evs[i])
+        step()
+    t_end.record(stream)
+    barrier()
+    kda.set_stage_events(None)
+    clk = clocks.stop()
+    kda.device_status(dev)
+    ms_total = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    stage_ms = {"schedule": [], "chunk": [], "recurrence": []}
+    for row in evs:
+        stage_ms["schedule"].append(row[0].elapsed_time(row[1]))
+        stage_ms["chunk"].append(row[1].elapsed_time(row[2]))
+        stage_ms["recurrence"].append(row[2].elapsed_time(row[3]))
+    stage_avg = {k: sum(v) / len(v) for k, v in stage_ms.items()}
+
+    # end to end: pinned host inputs -> device -> fwd -> outputs back to pinned host
+    host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hT_h = None if hT is None else torch.empty(hT.shape, dtype=hT.dtype, pin_memory=True)
+    in_keys = [k for k in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state",
+                           "cu_seqlens") if host.get(k) is not None]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in in_keys)
+    d2h = out.numel() * out.element_size() + (0 if hT is None else hT.numel() * hT.element_size())
+
+    def e2e_step():
+        for k in in_keys:
+            d[k].copy_(host[k], non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        if hT is not None:
+            hT_h.copy_(hT, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    hbm_peak, bf16_peak, peak_kind = peaks()
+    dominant = max(("chunk", "recurrence"), key=lambda k: stage_avg[k])
+    dom_ms = stage_avg[dominant]
+    achieved = alg_bytes / (dom_ms * 1e-3) / 1e9
+    roofline_s = max(flops / (bf16_peak * 1e12), alg_bytes / (hbm_peak * 1e9))
+    traffic = None
+    src = {"chunk": "kda_prep.cu", "recurrence": "kda_recur.cu"}[dominant]
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(os.path.join(ROOT, "gated_delta_rule_30_gb300", "csrc", src), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        with open(tpath) as f:
+            tr = json.load(f).get(dominant, {})
+        if tr.get("source_sha256_16") == h and tr.get("workload") == args.workload:
+            traffic = tr.get("bytes_per_launch")
+
+    line = {
+        "metric": METRIC, "value": head_tokens * world / (ms_step * 1e-3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": p["B"], "T": p["T"], "H": p["H"], "K": D, "V": D,
+                   "seed": w.seed, "state_dtype": str(p["state_dtype"]).replace("torch.", ""),
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "l2": "inputs larger than L2 (%.2f GB per step vs 129 MB)" % (alg_bytes / 1e9),
+                   "head_tokens_per_step": head_tokens, "counted_flop_per_step": flops,
+                   "counted_bytes_per_step": alg_bytes},
+        "tflops": flops / (ms_step * 1e-3) / 1e12,
+        "roofline_fraction_step": roofline_s / (ms_step * 1e-3),
+        "stage_ms": stage_avg,
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                     "peak_kind": peak_kind,
+                     "note": "achieved = counted bytes of the whole pass / dominant kernel time"},
+        "e2e": {"value": head_tokens * world / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(p, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,1 +1,235 @@
-"""GB300-native Kimi Delta Attention forward pass (binding filled in below)."""
+"""GB300 (sm_103a) Kimi Delta Attention forward pass.
+
+Thin Python binding over the C ABI in ``include/kda.h`` (``libkda.so``, built
+in-tree by ``gated_delta_rule_30_gb300.build``).  This module only marshals
+arguments: it checks tensor shapes/dtypes/devices, passes raw device pointers
+and the current CUDA stream, and turns status codes into exceptions.  Every
+step of the computation runs in the library's CUDA kernels; there is no CPU or
+PyTorch fallback, and a missing library raises.
+
+``fwd`` follows the call printed in "Flashkda Delta Attention", section "Core
+Kernel API":
+
+    fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+        initial_state=None, final_state=None, cu_seqlens=None)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = ["fwd", "lib", "library_path", "workspace_size", "device_status", "KDAError",
+           "selftest_tcgen05"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libkda.so")
+_lib = None
+
+KDA_OK = 0
+_STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED",
+           3: "KDA_ERR_CUDA", 4: "KDA_ERR_TIMEOUT", 5: "KDA_ERR_DEVICE_INPUT"}
+DTYPE_NONE, DTYPE_BF16, DTYPE_FP32 = 0, 1, 2
+
+
+class KDAError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{_STATUS.get(code, code)}: {message}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """Load libkda.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()' or "
+                "python gated_delta_rule_30_gb300/build.py)")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i32, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+        fwd_args = [vp, vp, vp, vp, vp, f32, vp, vp, vp, f32, vp, ctypes.c_int, vp, ctypes.c_int,
+                    vp, i32, i32, i32, i32, i32, i32]
+        L.kda_fwd.restype = ctypes.c_int
+        L.kda_fwd.argtypes = fwd_args + [vp]
+        L.kda_fwd_ws.restype = ctypes.c_int
+        L.kda_fwd_ws.argtypes = fwd_args + [vp, ctypes.c_size_t, vp]
+        L.kda_workspace_size.restype = ctypes.c_size_t
+        L.kda_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        L.kda_device_status.restype = ctypes.c_int
+        L.kda_device_status.argtypes = [vp]
+        L.kda_status_string.restype = ctypes.c_char_p
+        L.kda_status_string.argtypes = [ctypes.c_int]
+        L.kda_last_error_message.restype = ctypes.c_char_p
+        L.kda_last_error_message.argtypes = []
+        L.kda_abi_version.restype = ctypes.c_int
+        L.kda_abi_version.argtypes = []
+        L.kda_set_stage_events.restype = ctypes.c_int
+        L.kda_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
+        L.kda_selftest_tcgen05.restype = ctypes.c_int
+        L.kda_selftest_tcgen05.argtypes = [vp, vp, vp, i32, i32, vp]
+        _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != KDA_OK:
+        msg = lib().kda_last_error_message()
+        raise KDAError(rc, msg.decode() if msg else "")
+
+
+def _stream_ptr(device):
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _state_dtype(t):
+    import torch
+    if t is None:
+        return DTYPE_NONE
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_FP32
+    raise TypeError(f"state dtype must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+_WS_CACHE = {}
+
+
+def workspace_size(B: int, T: int, H: int, num_seqs: int = 0, has_cu_seqlens: bool = False) -> int:
+    n = lib().kda_workspace_size(B, T, H, num_seqs, 1 if has_cu_seqlens else 0)
+    if n == 0:
+        _check(1)
+    return int(n)
+
+
+def _workspace(device, nbytes):
+    import torch
+    key = (device.type, device.index)
+    ws = _WS_CACHE.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _WS_CACHE[key] = ws
+    return ws
+
+
+def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
+        final_state=None, cu_seqlens=None, workspace=None):
+    """KDA forward pass on the GPU; writes ``out`` (and ``final_state``) in place.
+
+    q, k, g: bf16 [B, T, H, 128]; v, out: bf16 [B, T, H, 128]; beta: bf16 [B, T, H];
+    A_log: fp32 [H]; dt_bias: fp32 [H, 128]; initial_state / final_state:
+    [N, H, 128, 128] bf16 or fp32 (same dtype when both given) or None;
+    cu_seqlens: int32 [N + 1] on the device (requires B = 1) or None.
+    ``workspace``: optional uint8 device tensor of at least ``workspace_size``
+    bytes; by default a per-device buffer from torch's allocator is reused.
+    Returns ``out``.
+    """
+    import torch
+    L = lib()
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, K]")
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if k.shape != q.shape or g.shape != q.shape:
+        raise ValueError("k and g must have q's shape")
+    if tuple(v.shape) != (B, T, H, V) or tuple(out.shape) != (B, T, H, V):
+        raise ValueError("v and out must be [B, T, H, V]")
+    if tuple(beta.shape) != (B, T, H):
+        raise ValueError("beta must be [B, T, H]")
+    for name, t, shp in (("A_log", A_log, (H,)), ("dt_bias", dt_bias, (H, K))):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 \
+                or not t.is_contiguous() or tuple(t.shape) != shp:
+            raise ValueError(f"{name} must be a contiguous CUDA float32 tensor of shape {shp}")
+    num_seqs = 0
+    if cu_seqlens is not None:
+        if not cu_seqlens.is_cuda or cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 \
+                or not cu_seqlens.is_contiguous():
+            raise ValueError("cu_seqlens must be a contiguous 1-D int32 CUDA tensor")
+        num_seqs = cu_seqlens.numel() - 1
+    N = num_seqs if cu_seqlens is not None else B
+    for name, t in (("initial_state", initial_state), ("final_state", final_state)):
+        if t is not None:
+            if not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (N, H, K, V):
+                raise ValueError(f"{name} must be a contiguous CUDA tensor of shape {(N, H, K, V)}")
+    dev = q.device
+    stream = _stream_ptr(dev)
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out), _ptr(A_log),
+            _ptr(dt_bias), float(lower_bound), _ptr(initial_state), _state_dtype(initial_state),
+            _ptr(final_state), _state_dtype(final_state), _ptr(cu_seqlens), int(num_seqs), B, T,
+            H, K, V]
+    with torch.cuda.device(dev):
+        need = L.kda_workspace_size(B, T, H, num_seqs, 1 if cu_seqlens is not None else 0)
+        if need == 0:
+            _check(L.kda_fwd(*args, stream))  # reports the size error
+        ws = workspace if workspace is not None else _workspace(dev, need)
+        _check(L.kda_fwd_ws(*args, ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(ws.numel()),
+                            stream))
+    return out
+
+
+def fwd_alloc(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
+              final_state=None, cu_seqlens=None):
+    """As ``fwd`` but through ``kda_fwd`` (library-side stream-ordered scratch)."""
+    import torch
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    num_seqs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    with torch.cuda.device(q.device):
+        _check(lib().kda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                             _ptr(out), _ptr(A_log), _ptr(dt_bias), float(lower_bound),
+                             _ptr(initial_state), _state_dtype(initial_state), _ptr(final_state),
+                             _state_dtype(final_state), _ptr(cu_seqlens), int(num_seqs), B, T, H,
+                             K, V, _stream_ptr(q.device)))
+    return out
+
+
+def device_status(device=None):
+    """Synchronise the current stream and raise if a device-side check fired."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        _check(lib().kda_device_status(_stream_ptr(dev)))
+
+
+def set_stage_events(events):
+    """Record 4 CUDA events around the library's kernels in later calls (None: off).
+
+    ``events``: four ``torch.cuda.Event(enable_timing=True)`` objects; they mark
+    before schedule / after schedule / after the chunk kernel / after the
+    recurrence kernel on the call's stream.
+    """
+    L = lib()
+    if events is None:
+        _check(L.kda_set_stage_events(None, 0))
+        return
+    for e in events:
+        if e.cuda_event == 0:
+            raise ValueError("events must be created (record them once) before use")
+    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(L.kda_set_stage_events(arr, 4))
+
+
+def selftest_tcgen05(a, b, N, K):
+    """Run the tcgen05 operand-layout self-test (a: bf16 [128, K], b: bf16 [K, N], CUDA)."""
+    import torch
+    d = torch.empty((4, 128, N), dtype=torch.float32, device=a.device)
+    with torch.cuda.device(a.device):
+        _check(lib().kda_selftest_tcgen05(_ptr(a), _ptr(b), _ptr(d), N, K, _stream_ptr(a.device)))
+    return d

@@ -1,0 +1,443 @@
+// kda_recur.cu -- recurrence kernel of the KDA forward pass: the sequential
+// chunk-to-chunk state update for one (sequence, head, value slice).
+//
+// Per chunk, with S the K x VS state slice entering it (fp32, kept in TMEM:
+// lane = key channel, column = value channel) and the chunk record written by
+// the chunk kernel:
+//   X     = [W ; scale*Qhat] . S                  (tcgen05, M=128, K=128)
+//   Delta = U - X[0:64]                           (v_new, fp32 -> bf16)
+//   S     = Diag(exp(G_last)) S + Ktilde^T . Delta   (tcgen05, M=128, K=64)
+//   O     = X[64:128] + scale*Aqk . Delta         (tcgen05, accumulated in X;
+//                                                  Aqk as a bf16 hi + lo pair)
+// which is the unrolled gated delta rule over the chunk (reading of "Flashkda
+// Delta Attention", "Core Kernel API": recurrent state updates; the value
+// dimension splits exactly because column j of S, Delta and O depends only on
+// column j).  The decay is applied in TMEM while the bf16 snapshot of S used
+// by the first product is taken, so each chunk costs two dependent MMA
+// rounds.
+//
+// Warp roles (192 threads): warps 0-3 own the 4 TMEM lane quarters (state
+// snapshot / decay, Delta for rows 0-63, output rows 64-127, state I/O); warp
+// 4 streams records with bulk copies into a 2-stage ring; warp 5 issues the
+// MMAs.  Every mbarrier wait is bounded; on timeout the CTA records
+// kStatusTimeout, stops, waits (bounded) for its own copies and frees TMEM.
+#include <cuda_runtime.h>
+
+#include <type_traits>
+
+#include "kda_internal.h"
+#include "tc.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kThreads = 192;
+
+template <int VS>
+struct RecurLayout {
+    // the first kRecOperands bytes mirror the record: WQ, KT, AQ hi, AQ lo
+    static constexpr uint32_t kStageWQ = kRecWQ;
+    static constexpr uint32_t kStageKT = kRecKT;
+    static constexpr uint32_t kStageAQ = kRecAQ;
+    static constexpr uint32_t kStageAQL = kRecAQL;
+    static constexpr uint32_t kStageUT = kRecOperands;               // VS x 128 B
+    static constexpr uint32_t kStageGam = kRecOperands + VS * 128;   // 512 B
+    static constexpr uint32_t kStageBytes = kStageGam + 512;
+    static constexpr uint32_t kSb = 2 * kStageBytes;        // S snapshot, K=128 x N=VS, MN-major
+    static constexpr uint32_t kDb = kSb + VS * 256;         // Delta, K=64 x N=VS, MN-major
+    static constexpr uint32_t kBytes = kDb + VS * 128;
+    static constexpr uint32_t kLoadBytes = kRecOperands + VS * 128 + 512;
+    static constexpr uint32_t kTmemCols = (3 * VS <= 128) ? 128 : (3 * VS <= 256 ? 256 : 512);
+};
+
+struct RecurArgs {
+    void* out;  // bf16 [tokens, H, 128]
+    const void* h0;
+    void* hT;
+    int H;
+    int N;
+    const int32_t* flags;
+    const int32_t* chunk_off;
+    const ChunkInfo* info;
+    const uint8_t* records;
+    int* status;
+};
+
+template <typename T>
+struct StateIO;
+template <>
+struct StateIO<float> {
+    static __device__ __forceinline__ void load16(const void* base, size_t off, uint32_t (&r)[16]) {
+        const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + off);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 x = p[i];
+            r[4 * i + 0] = __float_as_uint(x.x);
+            r[4 * i + 1] = __float_as_uint(x.y);
+            r[4 * i + 2] = __float_as_uint(x.z);
+            r[4 * i + 3] = __float_as_uint(x.w);
+        }
+    }
+    static __device__ __forceinline__ void store16(void* base, size_t off, const uint32_t (&r)[16]) {
+        float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + off);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            p[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                               __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+    }
+};
+template <>
+struct StateIO<__nv_bfloat16> {
+    static __device__ __forceinline__ void load16(const void* base, size_t off, uint32_t (&r)[16]) {
+        const uint4* p =
+            reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(base) + off);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint4 x = p[i];
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                r[8 * i + 2 * j] = __float_as_uint(bf16_lo(w[j]));
+                r[8 * i + 2 * j + 1] = __float_as_uint(bf16_hi(w[j]));
+            }
+        }
+    }
+    static __device__ __forceinline__ void store16(void* base, size_t off, const uint32_t (&r)[16]) {
+        uint4* p = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) + off);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            p[i] = make_uint4(pack_bf16(__uint_as_float(r[8 * i + 0]), __uint_as_float(r[8 * i + 1])),
+                              pack_bf16(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
+                              pack_bf16(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
+                              pack_bf16(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+    }
+};
+struct NoState {};
+
+// H0 / HT: float, __nv_bfloat16 or NoState
+template <int VS, typename H0, typename HT>
+__global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
+    using L = RecurLayout<VS>;
+    constexpr int kSlices = kDim / VS;
+    extern __shared__ __align__(1024) uint8_t sm[];
+    __shared__ uint64_t full[2], empty[2], s_ready, mma1, d_ready, mma2;
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_abort;
+
+    if (P.flags[0] != 1) return;
+    // a CTA that already gave up on a bounded wait poisons the launch: skip the rest
+    if (*((volatile int*)P.status) & kStatusTimeout) return;
+    const int H = P.H;
+    const int slice = blockIdx.x % kSlices;
+    const int nh = blockIdx.x / kSlices;
+    const int h = nh % H;
+    const int n = nh / H;
+    const int v0 = slice * VS;
+    const int c_begin = P.chunk_off[n];
+    const int nchunks = P.chunk_off[n + 1] - c_begin;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---------------------------------------------------------------- set-up
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, L::kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_init(&empty[0], 1);
+        mbar_init(&empty[1], 1);
+        mbar_init(&s_ready, 128);
+        mbar_init(&mma1, 1);
+        mbar_init(&d_ready, 64);
+        mbar_init(&mma2, 1);
+        mbar_fence_init();
+        s_abort = 0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base;
+    const uint32_t tS = tbase;  // columns [0, VS)
+    const size_t state_base = ((size_t)n * H + h) * kDim * kDim;
+
+    // initial state -> TMEM (thread = key channel)
+    if (warp < 4) {
+        const int ch = tid;
+#pragma unroll
+        for (int c0 = 0; c0 < VS; c0 += 16) {
+            uint32_t r[16];
+            if constexpr (std::is_same<H0, NoState>::value) {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) r[u] = 0u;
+            } else {
+                StateIO<H0>::load16(P.h0, state_base + (size_t)ch * kDim + v0 + c0, r);
+            }
+            tmem_st16(taddr(tS, 32u * warp, (uint32_t)c0), r);
+        }
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int fills[2] = {0, 0};
+            for (int i = 0; i < nchunks; ++i) {
+                const int s = i & 1;
+                if (fills[s] > 0 && !mbar_wait(&empty[s], (uint32_t)((fills[s] - 1) & 1))) {
+                    atomicOr(P.status, kStatusTimeout);
+                    s_abort = 1;
+                    break;
+                }
+                if (*((volatile int*)&s_abort)) break;
+                uint8_t* st = sm + s * L::kStageBytes;
+                const uint8_t* rec = P.records + ((size_t)(c_begin + i) * H + h) * kRecBytes;
+                mbar_arrive_expect_tx(&full[s], L::kLoadBytes);
+                bulk_g2s(st, rec, kRecOperands, &full[s]);
+                bulk_g2s(st + L::kStageUT, rec + kRecUT + v0 * 128, VS * 128, &full[s]);
+                bulk_g2s(st + L::kStageGam, rec + kRecGam, 512, &full[s]);
+                ++fills[s];
+            }
+            // drain: every issued fill must have landed before the CTA exits
+            for (int s = 0; s < 2; ++s)
+                if (fills[s] > 0 && !mbar_wait(&full[s], (uint32_t)((fills[s] - 1) & 1)))
+                    atomicOr(P.status, kStatusTimeout);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc1 = idesc_bf16_f32(128, VS, true, true);
+            const uint32_t idesc2 = idesc_bf16_f32(128, VS, false, true);
+            const uint32_t sb = smem_addr(sm + L::kSb);
+            const uint32_t db = smem_addr(sm + L::kDb);
+            for (int i = 0; i < nchunks; ++i) {
+                const int s = i & 1;
+                const uint32_t ph = (uint32_t)(i & 1);
+                const uint32_t tX = tbase + VS * (1 + (i & 1));
+                const uint32_t st = smem_addr(sm + s * L::kStageBytes);
+                if (!mbar_wait(&full[s], (uint32_t)((i >> 1) & 1)) || !mbar_wait(&s_ready, ph)) {
+                    atomicOr(P.status, kStatusTimeout);
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tX, smem_desc(st + L::kStageWQ + kk * 256, 128, 2048),
+                             smem_desc(sb + kk * 256, 128, 2048), idesc1, kk > 0 ? 1u : 0u);
+                mma_commit(&mma1);
+                if (!mbar_wait(&d_ready, ph)) {
+                    atomicOr(P.status, kStatusTimeout);
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tS, smem_desc(st + L::kStageKT + kk * 256, 128, 1024),
+                             smem_desc(db + kk * 256, 128, 1024), idesc2, 1u);
+                // [* ; Aqk_hi] and [* ; Aqk_lo]: rows 0..63 start 8 KB before the
+                // data and only touch X rows 0..63, which are dead once Delta is formed
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tX, smem_desc(st + L::kStageAQ - 8192 + kk * 256, 128, 1024),
+                             smem_desc(db + kk * 256, 128, 1024), idesc2, 1u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tX, smem_desc(st + L::kStageAQL - 8192 + kk * 256, 128, 1024),
+                             smem_desc(db + kk * 256, 128, 1024), idesc2, 1u);
+                mma_commit(&mma2);
+                mma_commit(&empty[s]);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ state / epilogue warps
+        const int row = tid;  // TMEM lane: key channel for S, token row for X
+        int prev_tok0 = 0, prev_len = 0;
+        auto store_output = [&](int i_prev) {
+            // rows 64..127 of X[i_prev & 1] hold the outputs of chunk i_prev
+            const int t = row - 64;
+            const uint32_t tX = tbase + VS * (1 + (i_prev & 1));
+#pragma unroll
+            for (int c0 = 0; c0 < VS; c0 += 16) {
+                uint32_t r[16];
+                tmem_load16(taddr(tX, 32u * warp, (uint32_t)c0), r);
+                if (t < prev_len) {
+                    uint4* dst = reinterpret_cast<uint4*>(
+                        reinterpret_cast<__nv_bfloat16*>(P.out) +
+                        ((size_t)(prev_tok0 + t) * H + h) * kDim + v0 + c0);
+                    dst[0] = make_uint4(pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1])),
+                                        pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3])),
+                                        pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5])),
+                                        pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7])));
+                    dst[1] = make_uint4(pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9])),
+                                        pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11])),
+                                        pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13])),
+                                        pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15])));
+                }
+            }
+        };
+        for (int i = 0; i < nchunks; ++i) {
+            const int s = i & 1;
+            const uint32_t ph = (uint32_t)(i & 1);
+            const uint8_t* st = sm + s * L::kStageBytes;
+            if (!mbar_wait(&full[s], (uint32_t)((i >> 1) & 1))) {
+                atomicOr(P.status, kStatusTimeout);
+                s_abort = 1;
+                break;
+            }
+            // snapshot S (bf16, MN-major B operand K=128 x N=VS) and decay it in TMEM
+            {
+                const float gam = reinterpret_cast<const float*>(st + L::kStageGam)[row];
+#pragma unroll
+                for (int c0 = 0; c0 < VS; c0 += 16) {
+                    uint32_t r[16];
+                    tmem_load16(taddr(tS, 32u * warp, (uint32_t)c0), r);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t* x = r + 8 * half;
+                        st_shared_v4(smem_addr(sm + L::kSb +
+                                               mnmaj_off(c0 + 8 * half, row, 128, 2048)),
+                                     pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                                     pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                                     pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                                     pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
+                    }
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * gam);
+                    tmem_st16(taddr(tS, 32u * warp, (uint32_t)c0), r);
+                }
+                tmem_wait_st();
+                fence_async_smem();
+                tc_fence_before();
+                mbar_arrive(&s_ready);
+            }
+            if (warp >= 2) {
+                if (i > 0) store_output(i - 1);
+            } else {
+                // Delta = U - X[0:64] for token row `row`
+                if (!mbar_wait(&mma1, ph)) {
+                    atomicOr(P.status, kStatusTimeout);
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tX = tbase + VS * (1 + (i & 1));
+                const uint16_t* ut = reinterpret_cast<const uint16_t*>(st + L::kStageUT);
+#pragma unroll
+                for (int c0 = 0; c0 < VS; c0 += 16) {
+                    uint32_t r[16];
+                    tmem_load16(taddr(tX, 32u * warp, (uint32_t)c0), r);
+                    float d[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u)
+                        d[u] = bf16_to_f(ut[(c0 + u) * 64 + row]) - __uint_as_float(r[u]);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half)
+                        st_shared_v4(smem_addr(sm + L::kDb +
+                                               mnmaj_off(c0 + 8 * half, row, 128, 1024)),
+                                     pack_bf16(d[8 * half + 0], d[8 * half + 1]),
+                                     pack_bf16(d[8 * half + 2], d[8 * half + 3]),
+                                     pack_bf16(d[8 * half + 4], d[8 * half + 5]),
+                                     pack_bf16(d[8 * half + 6], d[8 * half + 7]));
+                }
+                fence_async_smem();
+                tc_fence_before();
+                mbar_arrive(&d_ready);
+            }
+            if (!mbar_wait(&mma2, ph)) {
+                atomicOr(P.status, kStatusTimeout);
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const ChunkInfo ci = P.info[c_begin + i];
+            prev_tok0 = ci.tok0;
+            prev_len = ci.len;
+        }
+        if (!*((volatile int*)&s_abort)) {
+            if (warp >= 2 && nchunks > 0) store_output(nchunks - 1);
+            if constexpr (!std::is_same<HT, NoState>::value) {
+                const int ch = row;
+#pragma unroll
+                for (int c0 = 0; c0 < VS; c0 += 16) {
+                    uint32_t r[16];
+                    tmem_load16(taddr(tS, 32u * warp, (uint32_t)c0), r);
+                    StateIO<HT>::store16(P.hT, state_base + (size_t)ch * kDim + v0 + c0, r);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, L::kTmemCols);
+}
+
+template <int VS, typename H0, typename HT>
+cudaError_t launch_recur_t(const Problem& p, const RecurArgs& a, cudaStream_t st) {
+    using L = RecurLayout<VS>;
+    auto kern = recur_kernel<VS, H0, HT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    const long long blocks = (long long)p.N * p.H * (kDim / VS);
+    kern<<<(unsigned)blocks, kThreads, L::kBytes, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int VS, typename H0>
+cudaError_t launch_recur_h0(const Problem& p, const RecurArgs& a, cudaStream_t st) {
+    switch (p.hT_dtype) {
+        case KDA_DTYPE_FP32: return launch_recur_t<VS, H0, float>(p, a, st);
+        case KDA_DTYPE_BF16: return launch_recur_t<VS, H0, __nv_bfloat16>(p, a, st);
+        default: return launch_recur_t<VS, H0, NoState>(p, a, st);
+    }
+}
+
+template <int VS>
+cudaError_t launch_recur_vs(const Problem& p, const RecurArgs& a, cudaStream_t st) {
+    switch (p.h0_dtype) {
+        case KDA_DTYPE_FP32: return launch_recur_h0<VS, float>(p, a, st);
+        case KDA_DTYPE_BF16: return launch_recur_h0<VS, __nv_bfloat16>(p, a, st);
+        default: return launch_recur_h0<VS, NoState>(p, a, st);
+    }
+}
+
+}  // namespace
+
+int recur_slice_width(const Problem& p, int num_sms) {
+    // Split the value dimension only as far as needed to fill the GPU: each
+    // slice re-reads the shared operands of its chunk, so fewer slices means
+    // less on-chip traffic.
+    const long long pairs = (long long)p.N * p.H;
+    if (pairs >= 2LL * num_sms) return 128;
+    if (pairs * 2 >= num_sms) return 64;
+    return 32;
+}
+
+cudaError_t launch_recur(const Problem& p, const Workspace& ws, int* status, cudaStream_t st) {
+    if (p.N == 0 || p.H == 0) return cudaSuccess;
+    RecurArgs a;
+    a.out = p.out;
+    a.h0 = p.h0;
+    a.hT = p.hT;
+    a.H = p.H;
+    a.N = p.N;
+    a.flags = ws.flags;
+    a.chunk_off = ws.chunk_off;
+    a.info = ws.info;
+    a.records = ws.records;
+    a.status = status;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    switch (recur_slice_width(p, sms)) {
+        case 128: return launch_recur_vs<128>(p, a, st);
+        case 64: return launch_recur_vs<64>(p, a, st);
+        default: return launch_recur_vs<32>(p, a, st);
+    }
+}
+
+}  // namespace kda

@@ -5,7 +5,8 @@ arithmetic, and both the CUDA path and the fp64 oracle consume exactly the
 tensors it returns.  All draws come from one CPU ``torch.Generator`` seeded
 with ``seed``, in this order:
 
-1. (packed/varlen only) sequence lengths ``randint(lo, hi + 1, (N,))`` and
+1. (packed/varlen only) sequence lengths ``randint(lo, hi + 1, (N,))`` (or
+   the explicit ``lens`` of a custom workload, with no draw) and
    ``cu_seqlens = [0, cumsum(lens)]`` (int32);
 2. ``q``, ``k``: ``randn(B, T, H, K)`` in fp32, L2-normalised over the last
    dimension in fp32, then rounded once to bf16;
@@ -42,6 +43,7 @@ class Workload:
     len_range: tuple | None = None  # packed: (lo, hi) inclusive
     state_dtype: torch.dtype | None = None
     lower_bound: float = -5.0
+    lens: tuple | None = None       # packed with explicit lengths (no length draw)
     extra: dict = field(default_factory=dict)
 
 
@@ -56,6 +58,9 @@ WORKLOADS = {
     "state_io": Workload("state_io: 1024 seqs U[1,128] H=32, fp32 state", 1, None, 32, 4,
                          n_seqs=1024, len_range=(1, 128), state_dtype=torch.float32),
 }
+# smaller instance of long_context used for profiler captures (inputs still exceed L2)
+WORKLOADS["long_context_8k"] = Workload("long_context_8k: B=1 T=8192 H=32, fp32 state", 1, 8192,
+                                        32, 3, state_dtype=torch.float32)
 WORKLOAD_ORDER = ["ref_small", "dense_prefill", "varlen_packed", "long_context", "state_io"]
 
 
@@ -74,12 +79,16 @@ def make(w: Workload, K: int = K_DIM, V: int = V_DIM) -> dict:
     """Draw the workload's tensors on the CPU (see module docstring)."""
     gen = torch.Generator(device="cpu").manual_seed(w.seed)
     cu = None
-    if w.n_seqs is not None:
-        lo, hi = w.len_range
-        lens = torch.randint(lo, hi + 1, (w.n_seqs,), generator=gen, dtype=torch.int64)
-        cu = torch.zeros(w.n_seqs + 1, dtype=torch.int64)
+    if w.lens is not None or w.n_seqs is not None:
+        if w.lens is not None:
+            lens = torch.tensor(list(w.lens), dtype=torch.int64)
+        else:
+            lo, hi = w.len_range
+            lens = torch.randint(lo, hi + 1, (w.n_seqs,), generator=gen, dtype=torch.int64)
+        N = int(lens.numel())
+        cu = torch.zeros(N + 1, dtype=torch.int64)
         cu[1:] = torch.cumsum(lens, 0)
-        B, T, N = 1, int(cu[-1]), w.n_seqs
+        B, T = 1, int(cu[-1])
         cu = cu.to(torch.int32)
     else:
         B, T, N = w.B, w.T, w.B

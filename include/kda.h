@@ -1,0 +1,164 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward pass.
+ *
+ * The entry point mirrors the call printed in "Flashkda Delta Attention",
+ * section "Core Kernel API":
+ *     fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+ *         initial_state=None, final_state=None, cu_seqlens=None)
+ * with the constraints of "MoonshotAI/FlashKDA" (trend summary), section
+ * "Kernel API and Constraints": K = V = 128, cu_seqlens only with B = 1,
+ * states bf16, fp32 or absent and of matching dtype when both are given;
+ * activations are bf16 ("Flashkda Delta Attention", opening summary).
+ *
+ * Operation (per sequence n and head h; the pages print no formula, so the
+ * plain gated-delta-rule reading is taken and the gate form is a reading of
+ * the parameter names A_log, dt_bias, lower_bound):
+ *     la_t = max(-exp(A_log[h]) * softplus(g_t + dt_bias[h]), lower_bound)
+ *     S_t  = (I - beta_t k_t k_t^T) Diag(exp(la_t)) S_{t-1} + beta_t k_t v_t^T
+ *     o_t  = scale * S_t^T q_t
+ * S_0 = initial_state[n, h] (or 0); final_state[n, h] = S at the sequence end.
+ * q and k are used as given (no normalisation inside the call).
+ *
+ * Every pointer handed to kda_fwd is DEVICE memory owned by the caller; the
+ * call reads the inputs, writes out (and final_state) and keeps no reference
+ * after it returns.  The call is asynchronous on `stream`: it returns once the
+ * work is enqueued.  Scratch memory for the per-chunk intermediates is taken
+ * from the stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on
+ * `stream`) unless the caller supplies a workspace through kda_fwd_ws.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_ABI_VERSION 1
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARGUMENT = 1, /* bad shape / dtype / pointer; nothing launched */
+    KDA_ERR_UNSUPPORTED = 2,      /* valid but outside the kernels' range (e.g. lower_bound) */
+    KDA_ERR_CUDA = 3,             /* a CUDA runtime call failed; see kda_last_error_message */
+    KDA_ERR_TIMEOUT = 4,          /* a bounded device-side wait gave up (reported by kda_device_status) */
+    KDA_ERR_DEVICE_INPUT = 5      /* malformed device-side input (cu_seqlens) detected on the device */
+} kda_status_t;
+
+typedef enum {
+    KDA_DTYPE_NONE = 0, /* state absent */
+    KDA_DTYPE_BF16 = 1,
+    KDA_DTYPE_FP32 = 2
+} kda_dtype_t;
+
+/*
+ * kda_fwd -- KDA forward pass ("Flashkda Delta Attention", "Core Kernel API").
+ *
+ *   q, k, g     bf16 [B, T, H, K] contiguous (token-major; packed: B = 1, T = total)
+ *   v           bf16 [B, T, H, V]
+ *   beta        bf16 [B, T, H]
+ *   scale       output scale (commonly K^-0.5)
+ *   out         bf16 [B, T, H, V], written (round-to-nearest-even)
+ *   A_log       fp32 [H]
+ *   dt_bias     fp32 [H, K]
+ *   lower_bound clamp of the log-decay; finite, <= 0.  The kernels factor the
+ *               in-chunk decays around 16-token sub-blocks, which is exact in
+ *               fp32 for lower_bound >= -10; below that the call returns
+ *               KDA_ERR_UNSUPPORTED.
+ *   initial_state  [N, H, K, V] in initial_dtype, or NULL with KDA_DTYPE_NONE
+ *                  (zeros).  S[n][h][c][j]: key channel c, value channel j.
+ *   final_state    [N, H, K, V] in final_dtype, written, or NULL with
+ *                  KDA_DTYPE_NONE.  May alias initial_state exactly (in place);
+ *                  any other overlap is rejected.  When both states are given
+ *                  their dtypes must match.
+ *   cu_seqlens  int32 [num_seqs + 1] device offsets of packed sequences, or NULL
+ *               (then the B rows are the sequences).  Requires B = 1.  Must be
+ *               0 = cu[0] <= cu[1] <= ... <= cu[num_seqs] = T; zero-length
+ *               sequences are allowed (their final state is their initial
+ *               state).  A violation is detected on the device: the call then
+ *               skips all work and kda_device_status reports
+ *               KDA_ERR_DEVICE_INPUT.
+ *   num_seqs    number of packed sequences (ignored when cu_seqlens is NULL)
+ *   B, T, H, K, V  sizes; K = V = 128 is required, H >= 1, T >= 0, B >= 1.
+ *   stream      CUDA stream (cudaStream_t passed as void*; NULL = legacy default)
+ *
+ * N = num_seqs with cu_seqlens, else B.
+ * Returns KDA_OK once enqueued; argument errors are reported synchronously
+ * and launch nothing.
+ */
+kda_status_t kda_fwd(const void* q, const void* k, const void* v, const void* g,
+                     const void* beta, float scale, void* out, const float* A_log,
+                     const float* dt_bias, float lower_bound, const void* initial_state,
+                     kda_dtype_t initial_dtype, void* final_state, kda_dtype_t final_dtype,
+                     const int32_t* cu_seqlens, int32_t num_seqs, int32_t B, int32_t T,
+                     int32_t H, int32_t K, int32_t V, void* stream);
+
+/*
+ * kda_workspace_size -- bytes of device scratch kda_fwd_ws needs for a
+ * problem with these sizes (an upper bound that does not read cu_seqlens).
+ * Returns 0 and sets the error message for invalid sizes.
+ */
+size_t kda_workspace_size(int32_t B, int32_t T, int32_t H, int32_t num_seqs, int32_t has_cu_seqlens);
+
+/*
+ * kda_fwd_ws -- kda_fwd with caller-provided scratch: `workspace` is device
+ * memory of at least kda_workspace_size(...) bytes, 256-byte aligned, owned by
+ * the caller and not used by anything else until the enqueued work finishes.
+ * Makes no allocation.  Same arguments and errors as kda_fwd otherwise.
+ */
+kda_status_t kda_fwd_ws(const void* q, const void* k, const void* v, const void* g,
+                        const void* beta, float scale, void* out, const float* A_log,
+                        const float* dt_bias, float lower_bound, const void* initial_state,
+                        kda_dtype_t initial_dtype, void* final_state, kda_dtype_t final_dtype,
+                        const int32_t* cu_seqlens, int32_t num_seqs, int32_t B, int32_t T,
+                        int32_t H, int32_t K, int32_t V, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/*
+ * kda_device_status -- synchronises `stream`, then returns and clears the
+ * library's per-device status word: KDA_OK, KDA_ERR_DEVICE_INPUT (malformed
+ * cu_seqlens seen by an earlier call) or KDA_ERR_TIMEOUT (a bounded
+ * device-side wait gave up; that call's outputs are undefined).
+ */
+kda_status_t kda_device_status(void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* kda_status_string(kda_status_t status);
+
+/* Detail of the last error returned on the calling host thread (thread-local). */
+const char* kda_last_error_message(void);
+
+/* KDA_ABI_VERSION of the built library. */
+int kda_abi_version(void);
+
+/*
+ * kda_set_stage_events -- timing hook (no counterpart on the pages).  With
+ * count = 4, every later kda_fwd / kda_fwd_ws call on this process records
+ * events[0] before its first kernel, events[1] after the chunk-schedule
+ * kernel, events[2] after the chunk kernel and events[3] after the recurrence
+ * kernel, all on the call's stream (events are cudaEvent_t created by the
+ * caller and must outlive the calls).  count = 0 (or events = NULL) turns the
+ * hook off.  Not thread-safe; intended for benchmarks.
+ */
+kda_status_t kda_set_stage_events(void* const* events, int32_t count);
+
+/*
+ * kda_selftest_tcgen05 -- diagnostic for the tensor-core building blocks the
+ * kernels use (no counterpart on the pages).  Runs one M=128 x N x K bf16 MMA
+ * per operand-layout combination (A and B each K-major or MN-major, no
+ * swizzle) on device inputs a [128][K] and b [K][N] (row-major bf16), writing
+ * d [4][128][N] fp32 (one product per combination, in the order
+ * (A K-major, B K-major), (A MN, B MN), (A K, B MN), (A MN, B K)).
+ * N must be a multiple of 16 in [16, 256], K a multiple of 16 in [16, 128].
+ * Synchronous (returns after the kernel finishes).
+ */
+kda_status_t kda_selftest_tcgen05(const void* a, const void* b, float* d, int32_t N, int32_t K,
+                                  void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

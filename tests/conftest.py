@@ -17,3 +17,13 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def kda_lib():
+    """The CUDA library, built in-tree if it is missing or stale."""
+    from gated_delta_rule_30_gb300 import build
+    build.build()
+    import gated_delta_rule_30_gb300 as kda
+    kda.lib()
+    return kda

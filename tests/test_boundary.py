@@ -1,0 +1,104 @@
+"""C ABI boundary checks that need no GPU: the library loads, exports every
+function declared in include/*.h, and rejects bad arguments synchronously
+(before touching CUDA) with the documented status codes."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def declared_functions():
+    names = set()
+    for path in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(path).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(kda_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("kda_fwd", "kda_fwd_ws", "kda_workspace_size", "kda_device_status",
+              "kda_status_string", "kda_last_error_message", "kda_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(kda_lib):
+    L = ctypes.CDLL(kda_lib.library_path())
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, f"not exported: {missing}"
+    assert L.kda_abi_version() == 1
+
+
+def call(kda_lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=0.088, out=FAKE, A_log=FAKE,
+             dt_bias=FAKE, lb=-5.0, h0=None, h0d=0, hT=None, hTd=0, cu=None, ns=0, B=1, T=64,
+             H=2, K=128, V=128)
+    a.update(over)
+    L = kda_lib.lib()
+    rc = L.kda_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["out"], a["A_log"],
+                   a["dt_bias"], a["lb"], a["h0"], a["h0d"], a["hT"], a["hTd"], a["cu"], a["ns"],
+                   a["B"], a["T"], a["H"], a["K"], a["V"], None)
+    return rc, L.kda_last_error_message().decode()
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(K=64), 1), (dict(V=256), 1), (dict(H=0), 1), (dict(T=-1), 1), (dict(B=0), 1),
+    (dict(B=2, cu=FAKE, ns=2), 1),                        # cu_seqlens needs B == 1
+    (dict(h0=FAKE, h0d=1, hT=FAKE + (1 << 24), hTd=2), 1),  # state dtypes differ
+    (dict(h0=FAKE, h0d=3), 1),                            # bad dtype code
+    (dict(h0=FAKE, h0d=0), 1),                            # pointer without dtype
+    (dict(h0=None, h0d=2), 1),                            # dtype without pointer
+    (dict(lb=0.5), 1), (dict(lb=float("nan")), 1), (dict(lb=float("-inf")), 1),
+    (dict(lb=-10.5), 2),                                  # outside the supported range
+    (dict(scale=float("inf")), 1),
+    (dict(q=None), 1), (dict(out=None), 1), (dict(A_log=None), 1),
+    (dict(q=FAKE + 8), 1),                                # misaligned
+    (dict(h0=FAKE, h0d=2, hT=FAKE + 4096, hTd=2), 1),     # partial overlap of the states
+    (dict(cu=FAKE + 2, ns=1), 1),                         # misaligned cu_seqlens
+    (dict(cu=FAKE, ns=-1), 1),
+])
+def test_invalid_arguments_rejected(kda_lib, over, code):
+    rc, msg = call(kda_lib, **over)
+    assert rc == code, (rc, msg)
+    assert msg
+
+
+def test_status_strings(kda_lib):
+    L = kda_lib.lib()
+    assert L.kda_status_string(0) == b"KDA_OK"
+    assert L.kda_status_string(2) == b"KDA_ERR_UNSUPPORTED"
+    assert L.kda_status_string(99) == b"KDA_ERR_UNKNOWN"
+
+
+def test_workspace_size(kda_lib):
+    L = kda_lib.lib()
+    rec = 82432
+    # dense: N * ceil(T/64) chunks bound = (B*T + 63 B) / 64
+    n = L.kda_workspace_size(8, 2048, 16, 0, 0)
+    assert n >= 8 * 32 * 16 * rec
+    assert n < 8 * 33 * 16 * rec + 1 << 20
+    assert L.kda_workspace_size(2, 64, 1, 3, 1) == 0   # cu_seqlens needs B == 1
+    assert L.kda_workspace_size(1, 100, 2, 3, 1) > 0
+
+
+def test_stage_events_validation(kda_lib):
+    L = kda_lib.lib()
+    assert L.kda_set_stage_events(None, 0) == 0
+    arr = (ctypes.c_void_p * 3)()
+    assert L.kda_set_stage_events(arr, 3) == 1
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import gated_delta_rule_30_gb300 as kda
+    monkeypatch.setattr(kda, "_lib", None)
+    monkeypatch.setattr(kda, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        kda.lib()

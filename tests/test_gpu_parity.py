@@ -1,0 +1,211 @@
+"""Parity of the CUDA path with the fp64 oracle (GPU).
+
+Every case draws seeded inputs with ``gated_delta_rule_30_gb300.inputs``,
+runs ``kda.fwd`` (through the C ABI) and compares the bf16 outputs and the
+final states with the oracle over the whole tensors: relative Frobenius error
+<= 5e-3 and max-abs error <= 3e-2.  Full-size workloads compare every output
+of a sample of heads (the oracle computes (sequence, head) pairs
+independently, so a head subset is an exact sub-problem).
+"""
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_rule_30_gb300 import inputs
+from kda_testutil import (REC_BYTES, assert_close, decode_record, errors, read_schedule, run_gpu,
+                          run_oracle, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def make(name, **kw):
+    w = inputs.WORKLOADS[name]
+    if kw:
+        w = inputs.shrink(w, **kw)
+    return inputs.make(w)
+
+
+def custom(T=None, lens=None, H=2, state=torch.float32, seed=7, lower_bound=-5.0, B=1):
+    """Same recipe as the named workloads, with explicit sizes / lengths."""
+    w = inputs.Workload("custom", B, T, H, seed, state_dtype=state, lower_bound=lower_bound,
+                        lens=None if lens is None else tuple(lens))
+    return inputs.make(w)
+
+
+def check(oracle_mod, p, final_dtype="same", heads=None, what="", via_alloc=False):
+    out, hT = run_gpu(p, final_dtype, via_alloc=via_alloc)
+    o_ref, h_ref = run_oracle(oracle_mod, p, heads)
+    if heads is not None:
+        out = out.index_select(2, torch.tensor(heads))
+        hT = None if hT is None else hT.index_select(1, torch.tensor(heads))
+    eo = errors(out.reshape(o_ref.shape), o_ref)
+    es = errors(hT, h_ref) if hT is not None else None
+    print(f"\n[parity] {what}: out rel_fro={eo[0]:.3e} max_abs={eo[1]:.3e}"
+          + (f"; state rel_fro={es[0]:.3e} max_abs={es[1]:.3e}" if es else ""))
+    res = {"out": assert_close(out.reshape(o_ref.shape), o_ref, f"{what} out")}
+    if hT is not None:
+        res["state"] = assert_close(hT, h_ref, f"{what} final_state")
+    return res
+
+
+# ----------------------------------------------------------------------------- stages
+
+def test_chunk_records_match_oracle_stages(kda_lib, oracle_mod):
+    """Decode the chunk kernel's records and compare with the oracle's chunk form."""
+    import gated_delta_rule_30_gb300 as kda
+    p = custom(lens=[70, 5, 64, 129], H=3, state=None, seed=11)
+    N, H = p["N"], p["H"]
+    T = p["T"]
+    max_chunks = (T + 63 * N) // 64
+    ws = torch.zeros(kda.workspace_size(1, T, H, N, True), dtype=torch.uint8, device="cuda")
+    run_gpu(p, None, workspace=ws)
+    flags, chunk_off, info, off_rec = read_schedule(ws, N, max_chunks)
+    assert flags == 1
+    lens = [70, 5, 64, 129]
+    exp_chunks = [int(np.ceil(x / 64)) for x in lens]
+    assert list(chunk_off) == list(np.concatenate([[0], np.cumsum(exp_chunks)]))
+    raw = ws.cpu().numpy()
+    la_all = oracle_mod.log_decay(p["g"][0], p["A_log"], p["dt_bias"], p["lower_bound"])
+    scale = p["scale"]
+    for c in range(int(chunk_off[-1])):
+        tok0, L = int(info[c, 0]), int(info[c, 1])
+        assert 1 <= L <= 64
+        for h in range(H):
+            rec = raw[off_rec + (c * H + h) * REC_BYTES: off_rec + (c * H + h + 1) * REC_BYTES]
+            d = decode_record(rec)
+            sl = slice(tok0, tok0 + L)
+            q = p["q"][0, sl, h].double().numpy()
+            k = p["k"][0, sl, h].double().numpy()
+            v = p["v"][0, sl, h].double().numpy()
+            b = p["beta"][0, sl, h].double().numpy()
+            la = la_all[sl, h]
+            st = oracle_mod.chunk_stage(q, k, v, la, b)
+            E = np.exp(st["G"])
+            Ftil = np.exp(st["G"][-1][None, :] - st["G"])
+            tag = f"chunk {c} head {h} len {L}"
+            for name, gpu, ref in (("W", d["W"][:L], st["W"]), ("U", d["U"][:L], st["U"]),
+                                   ("Qhat", d["Qhat"][:L], scale * q * E),
+                                   ("Ktil", d["Ktil"][:L], k * Ftil),
+                                   ("Aqk", d["Aqk"][:L, :L], scale * st["Aqk"])):
+                rel, mx = errors(gpu, ref)
+                print(f"\n[stage] {tag} {name}: rel_fro={rel:.3e} max_abs={mx:.3e}")
+                assert rel < 1e-2, f"{tag} {name}: rel_fro {rel:.3e}"
+            np.testing.assert_allclose(d["gamma"], st["gamma"], rtol=1e-4, atol=1e-30,
+                                       err_msg=tag)
+            # padding rows/cols are exactly zero
+            assert np.all(d["W"][L:] == 0) and np.all(d["Qhat"][L:] == 0)
+            assert np.all(d["Ktil"][L:] == 0) and np.all(d["U"][L:] == 0)
+            assert np.all(d["Aqk"][L:] == 0) and np.all(d["Aqk"][:, L:] == 0)
+
+
+# ----------------------------------------------------------------------------- small cases
+
+def test_ref_small_full(kda_lib, oracle_mod):
+    check(oracle_mod, make("ref_small"), what="ref_small")
+
+
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 128, 129, 200])
+def test_ragged_lengths(kda_lib, oracle_mod, T):
+    check(oracle_mod, custom(T=T, H=2, seed=100 + T), what=f"T={T}")
+
+
+def test_packed_with_empty_sequences(kda_lib, oracle_mod):
+    p = custom(lens=[0, 5, 64, 0, 130, 1, 0], H=3, state=torch.bfloat16, seed=3)
+    check(oracle_mod, p, what="packed+empty")
+
+
+@pytest.mark.parametrize("h0,hT", [(None, None), (torch.float32, None), (None, torch.float32),
+                                   (None, torch.bfloat16), (torch.bfloat16, None),
+                                   (torch.bfloat16, torch.bfloat16),
+                                   (torch.float32, torch.float32)])
+def test_state_dtype_combinations(kda_lib, oracle_mod, h0, hT):
+    p = custom(T=150, H=2, state=h0, seed=21)
+    check(oracle_mod, p, final_dtype=hT, what=f"h0={h0} hT={hT}")
+
+
+def test_in_place_state(kda_lib, oracle_mod):
+    import gated_delta_rule_30_gb300 as kda
+    p = custom(lens=[33, 100, 64], H=2, state=torch.float32, seed=5)
+    o_ref, h_ref = run_oracle(oracle_mod, p)
+    d = to_dev(p)
+    out = torch.empty_like(d["v"])
+    st = d["initial_state"].clone()
+    kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], out, d["A_log"], d["dt_bias"],
+            d["lower_bound"], initial_state=st, final_state=st, cu_seqlens=d["cu_seqlens"])
+    kda.device_status()
+    assert_close(out.cpu().reshape(o_ref.shape), o_ref, "in-place out")
+    assert_close(st.cpu(), h_ref, "in-place state")
+
+
+@pytest.mark.parametrize("lb,A", [(0.0, None), (-1.0, None), (-10.0, 60.0), (-3.0, 60.0)])
+def test_lower_bound_range(kda_lib, oracle_mod, lb, A):
+    p = custom(T=192, H=2, seed=31, lower_bound=lb)
+    if A is not None:
+        p["A_log"] = torch.full_like(p["A_log"], A)  # every channel clamps at lower_bound
+    check(oracle_mod, p, what=f"lb={lb}")
+
+
+def test_one_hot_keys_overwrite(kda_lib, oracle_mod):
+    """beta = 1, no decay, permuted one-hot keys (exact in bf16): a repeated key
+    overwrites its slot; the query of that key reads the latest value."""
+    p = custom(T=96, H=1, state=None, seed=41, lower_bound=0.0)
+    gen = torch.Generator().manual_seed(0)
+    idx = torch.randint(0, 128, (96,), generator=gen)
+    keys = torch.nn.functional.one_hot(idx, 128).to(torch.bfloat16)
+    p["k"] = keys.reshape(1, 96, 1, 128).contiguous()
+    qi = torch.roll(idx, 3)
+    p["q"] = torch.nn.functional.one_hot(qi, 128).to(torch.bfloat16).reshape(1, 96, 1, 128)
+    p["beta"] = torch.ones(1, 96, 1, dtype=torch.bfloat16)
+    check(oracle_mod, p, what="one-hot")
+
+
+# ----------------------------------------------------------------------------- shrunk workloads
+
+def test_dense_prefill_shrunk(kda_lib, oracle_mod):
+    check(oracle_mod, make("dense_prefill", T=320, H=4), what="dense_prefill shrunk")
+
+
+def test_varlen_packed_shrunk(kda_lib, oracle_mod):
+    check(oracle_mod, make("varlen_packed", n_seqs=6, hi=300, H=4), what="varlen shrunk")
+
+
+def test_state_io_shrunk(kda_lib, oracle_mod):
+    check(oracle_mod, make("state_io", n_seqs=64, H=4), what="state_io shrunk")
+
+
+def test_alloc_entry_matches_workspace_entry(kda_lib, oracle_mod):
+    p = make("varlen_packed", n_seqs=4, hi=200, H=2)
+    o1, h1 = run_gpu(p)
+    o2, h2 = run_gpu(p, via_alloc=True)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_deterministic(kda_lib):
+    p = make("dense_prefill", T=256, H=2)
+    o1, h1 = run_gpu(p)
+    o2, h2 = run_gpu(p)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_malformed_cu_seqlens_reported(kda_lib):
+    import gated_delta_rule_30_gb300 as kda
+    p = custom(lens=[10, 20, 30], H=2, state=None, seed=1)
+    d = to_dev(p)
+    bad = torch.tensor([0, 20, 10, 60], dtype=torch.int32, device="cuda")  # decreasing
+    out = torch.zeros_like(d["v"])
+    kda.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], out, d["A_log"], d["dt_bias"],
+            d["lower_bound"], cu_seqlens=bad)
+    with pytest.raises(kda.KDAError) as ei:
+        kda.device_status()
+    assert ei.value.code == 5
+    assert torch.count_nonzero(out).item() == 0  # nothing was written
+    kda.device_status()  # cleared
+
+
+# ----------------------------------------------------------------------------- full sizes (sampled heads)
+
+@pytest.mark.parametrize("name,heads", [("dense_prefill", None), ("varlen_packed", [0, 13, 31]),
+                                        ("long_context", [0, 31]), ("state_io", [1, 30])])
+def test_full_size_workloads(kda_lib, oracle_mod, name, heads):
+    p = make(name)
+    check(oracle_mod, p, heads=heads, what=f"{name} full")
