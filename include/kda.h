@@ -117,6 +117,35 @@ kda_status_t kda_fwd_ws(const void* q, const void* k, const void* v, const void*
                         size_t workspace_bytes, void* stream);
 
 /*
+ * kda_fwd_noalloc -- kda_fwd for callers that must not allocate device memory
+ * during the call (no counterpart on the pages).  Some callers cannot: a
+ * serving runtime that reserves all GPU memory at start-up and forbids
+ * allocation on the request path, a plug-in running under memory pools it does
+ * not own, or real-time code that cannot pay for an allocator call.  This
+ * entry point allocates nothing: its scratch is a fixed area compiled into
+ * the library (kda_noalloc_scratch_bytes(), 64 MiB), which every GPU that
+ * loads the library holds until the process exits.  Inputs and outputs are
+ * the caller's, exactly as for kda_fwd.
+ *   - A problem whose kda_workspace_size exceeds the area is rejected with
+ *     KDA_ERR_UNSUPPORTED and a message giving both sizes.
+ *   - The first call on a device looks up the area's address on that device
+ *     (it must be the current device); make that first call before any stream
+ *     capture.
+ *   - All calls share the one area and it keeps the last call's contents;
+ *     calls whose GPU work overlaps (other streams or host threads) race on it
+ *     and must be serialised by the caller.
+ */
+kda_status_t kda_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
+                             const void* beta, float scale, void* out, const float* A_log,
+                             const float* dt_bias, float lower_bound, const void* initial_state,
+                             kda_dtype_t initial_dtype, void* final_state,
+                             kda_dtype_t final_dtype, const int32_t* cu_seqlens, int32_t num_seqs,
+                             int32_t B, int32_t T, int32_t H, int32_t K, int32_t V, void* stream);
+
+/* Size in bytes of the fixed scratch area kda_fwd_noalloc uses. */
+size_t kda_noalloc_scratch_bytes(void);
+
+/*
  * kda_device_status -- synchronises `stream`, then returns and clears the
  * library's per-device status word: KDA_OK, KDA_ERR_DEVICE_INPUT (malformed
  * cu_seqlens seen by an earlier call) or KDA_ERR_TIMEOUT (a bounded
