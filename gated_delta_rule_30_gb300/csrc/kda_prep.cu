@@ -11,23 +11,28 @@
 //   T         = (I + A)^-1 (unit lower triangular)
 //   W         = T diag(beta) (K o E),  U = T diag(beta) V
 // and writes W, scale*(Q o E), (K o F)^T, scale*Aqk (as a bf16 hi/lo pair),
-// U^T and exp(G_last) in
-// the layout of one record (see kda_internal.h).  This is the chunkwise form
-// of the gated delta rule (reading of "Flashkda Delta Attention", "Core Kernel
-// API"; the pages give only the call), with the exponentials of G differences
-// factored per 16-token sub-block so that no factor overflows fp32/bf16:
-// for rows in sub-block a the reference point is token m_a = 16a + 7,
+// U^T and exp(G_last) in the layout of one record (see kda_internal.h).  This
+// is the chunkwise form of the gated delta rule (reading of "Flashkda Delta
+// Attention", "Core Kernel API"; the pages give only the call), with the
+// exponentials of G differences factored per 16-token sub-block so that no
+// factor overflows fp32/bf16: for rows in sub-block a the reference point is
+// token m_a = 16a + 7,
 //   left_i  = x_i o exp(G_i - G_{m_a})     (x = k or q),
 //   right_j = k_j o exp(G_{m_a} - G_j)     (j < 16(a+1)),
 // so |exponent| <= 8 |lower_bound| inside a sub-block and <= 0 across them.
+// Every exp(G_i - G_j) is a product of the alphas between i and j, so the
+// only transcendentals are those of the gate itself.
 //
-// Work split (128 threads, thread = key channel): the gate, decays and every
-// scaled operand are elementwise over tokens for a fixed channel; the four
-// score products (one per row sub-block, M=128 rows = k and q rows of that
-// sub-block, N = 16(a+1) key tokens, K = 128 channels), and the two WY
-// products (M = 128 channels, N = 64 tokens, K = 64 tokens) run on tcgen05
-// with fp32 accumulators in TMEM; the triangular inverse is fp32 forward
-// substitution (thread j owns column j of T).
+// Work split (256 threads): for the gate, the decays and the scaled operands
+// thread (c, h) owns key channel c = tid % 128 and the 32 tokens of half
+// h = tid / 128 of the chunk (products that cross the halves are exchanged
+// through shared memory).  The four score products (one per row sub-block:
+// M = 128 rows = the k and q rows of that sub-block, N = 16(a+1) key tokens,
+// K = 128 channels) and the two WY products (M = 128 channels, N = 64 tokens,
+// K = 64 tokens) run on tcgen05 with fp32 accumulators in TMEM.  The
+// triangular inverse is blocked: the four 16 x 16 diagonal blocks by forward
+// substitution (one warp each), then the off-diagonal blocks level by level,
+// T_ab = -T_aa sum_{b<=c<a} A_ac T_cb, in fp32 shared memory.
 #include <cuda_runtime.h>
 
 #include "kda_internal.h"
@@ -36,17 +41,20 @@
 namespace kda {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 // shared memory map (bytes)
 constexpr uint32_t kSmQ = 0, kSmK = 16384, kSmV = 32768, kSmG = 49152;  // staging tiles [64][128]
-constexpr uint32_t kSmLeft = 0;       // 32 KB   (aliases staging after it is consumed)
+constexpr uint32_t kSmLeft = 0;       // 32 KB   (aliases staging once it is consumed)
 constexpr uint32_t kSmR = 32768;      // 40 KB   R_0..R_3
 constexpr uint32_t kSmVbT = 73728;    // 16 KB   (beta V)^T, K-major, M = 128 value channels, K = 64
 constexpr uint32_t kSmKbT = 90112;    // 16 KB   (beta K o E)^T
-constexpr uint32_t kSmA = 0;          // fp32 [64][kAStride] (aliases Left after the score MMAs)
-constexpr uint32_t kSmTT = 32768;     // 8 KB    T^T as MN-major B operand (aliases R)
 constexpr uint32_t kSmBytes = 106496;
-constexpr int kAStride = 68;
+// after the score MMAs (alias Left / R)
+constexpr int kStr = 68;              // fp32 row stride of the 64 x 64 tiles
+constexpr uint32_t kSmA = 0;          // A (beta-scaled, strictly lower), fp32 [64][kStr]
+constexpr uint32_t kSmT = 17408;      // T, fp32 [64][kStr]
+constexpr uint32_t kSmX = 34816;      // level products, fp32 [3][16][16]
+constexpr uint32_t kSmTT = 40960;     // T^T as MN-major B operand, bf16 8 KB
 // R_a (16(a+1) rows x 256 B) starts at 2048 a (a+1): 0, 4096, 12288, 24576
 __host__ __device__ constexpr uint32_t r_off(int a) { return 2048u * a * (a + 1); }
 // score block a occupies TMEM columns [8 a (a+1), 8 (a+1)(a+2)): 0, 16, 48, 96
@@ -75,14 +83,63 @@ struct PrepArgs {
 __device__ __forceinline__ float lds_bf16(const uint8_t* base, uint32_t off) {
     return bf16_to_f(*reinterpret_cast<const uint16_t*>(base + off));
 }
-
 __device__ __forceinline__ void stg_v4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+}
+__device__ __forceinline__ void sts_v4f(uint32_t saddr, const float (&x)[8]) {
+    st_shared_v4(saddr, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                 pack_bf16(x[6], x[7]));
+}
+__device__ __forceinline__ void stg_v4f(uint8_t* p, const float (&x)[8]) {
+    stg_v4(p, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+           pack_bf16(x[6], x[7]));
+}
+
+// Right factors of one sub-block pair owned by a half: for the local block
+// b0 (tokens 0..15 of the half, reference 7) and b1 (tokens 16..31,
+// reference 23), rf0[u] = exp(G_{7} - G_u) for u < 16 and rf1[u] =
+// exp(G_{23} - G_u) for u < 32 (local token indices).
+__device__ __forceinline__ void right_factors(const float (&al)[32], float (&rf0)[16],
+                                              float (&rf1)[32]) {
+    float run = 1.f;
+    rf0[7] = 1.f;
+#pragma unroll
+    for (int u = 6; u >= 0; --u) {
+        run *= al[u + 1];
+        rf0[u] = run;
+    }
+    run = 1.f;
+#pragma unroll
+    for (int u = 15; u > 7; --u) {
+        rf0[u] = run;
+        run *= al[u];
+    }
+    float inv = 1.f / run;
+#pragma unroll
+    for (int u = 8; u < 16; ++u) rf0[u] *= inv;
+    run = 1.f;
+    rf1[23] = 1.f;
+#pragma unroll
+    for (int u = 22; u >= 0; --u) {
+        run *= al[u + 1];
+        rf1[u] = run;
+    }
+    run = 1.f;
+#pragma unroll
+    for (int u = 31; u > 23; --u) {
+        rf1[u] = run;
+        run *= al[u];
+    }
+    inv = 1.f / run;
+#pragma unroll
+    for (int u = 24; u < 32; ++u) rf1[u] *= inv;
 }
 
 __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ float sBeta[kChunk];
+    __shared__ float sTot[2][kDim];   // product of each half's alphas
+    __shared__ float sQf[2][kDim];    // prod_{s=32}^{39} and prod_{s=32}^{55} alpha_s
     __shared__ uint64_t bar;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
@@ -97,23 +154,24 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
     const ChunkInfo ci = P.info[chunk];
     const int tok0 = ci.tok0, len = ci.len;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int ch = tid;
+    const int ch = tid & (kDim - 1);
+    const int half = tid >> 7;
+    const int t0 = 32 * half;  // first token of this thread's half
     uint8_t* rec = P.records + ((size_t)chunk * H + h) * kRecBytes;
 
     // ---------------------------------------------------------------- staging
     {
         const __nv_bfloat16* srcs[4] = {P.q, P.k, P.v, P.g};
-        const uint32_t dsts[4] = {kSmQ, kSmK, kSmV, kSmG};
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
 #pragma unroll
-            for (int it = 0; it < 8; ++it) {
+            for (int it = 0; it < 4; ++it) {
                 const int c = tid + kThreads * it;
                 const int row = c >> 4, col = c & 15;
                 const bool ok = row < len;
                 const __nv_bfloat16* src =
                     srcs[x] + ((size_t)(ok ? tok0 + row : tok0) * H + h) * kDim + col * 8;
-                cp_async16_zfill(sm + dsts[x] + row * 256 + col * 16, src, ok);
+                cp_async16_zfill(sm + x * 16384 + row * 256 + col * 16, src, ok);
             }
         }
         if (tid < kChunk)
@@ -134,92 +192,96 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
     }
     const uint32_t tbase = tmem_base;
 
-    // ---------------------------------------------------------------- gate + decays
-    float al[kChunk];
+    // ---------------------------------------------------------------- gate (32 tokens)
+    float al[32];
     {
         const float dtb = P.dt_bias[h * kDim + ch];
         const float negA = -__expf(P.A_log[h]);
         const float lb = P.lower_bound;
+        float prod = 1.f;
 #pragma unroll
-        for (int t = 0; t < kChunk; ++t) {
+        for (int u = 0; u < 32; ++u) {
+            const int t = t0 + u;
             const float x = lds_bf16(sm, kSmG + t * 256 + ch * 2) + dtb;
             const float sp = fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
             const float la = fmaxf(negA * sp, lb);
-            al[t] = (t < len) ? __expf(la) : 1.f;
+            al[u] = (t < len) ? __expf(la) : 1.f;
+            prod *= al[u];
+            if (half == 1 && u == 7) sQf[0][ch] = prod;   // prod_{32}^{39}
+            if (half == 1 && u == 23) sQf[1][ch] = prod;  // prod_{32}^{55}
         }
+        sTot[half][ch] = prod;
     }
-    uint32_t qp[kChunk / 2], kp[kChunk / 2];
+    uint32_t qp[16], kp[16];
 #pragma unroll
-    for (int t = 0; t < kChunk; t += 2) {
-        qp[t / 2] = pack_bf16(lds_bf16(sm, kSmQ + t * 256 + ch * 2),
+    for (int u = 0; u < 32; u += 2) {
+        const int t = t0 + u;
+        qp[u / 2] = pack_bf16(lds_bf16(sm, kSmQ + t * 256 + ch * 2),
                               lds_bf16(sm, kSmQ + (t + 1) * 256 + ch * 2));
-        kp[t / 2] = pack_bf16(lds_bf16(sm, kSmK + t * 256 + ch * 2),
+        kp[u / 2] = pack_bf16(lds_bf16(sm, kSmK + t * 256 + ch * 2),
                               lds_bf16(sm, kSmK + (t + 1) * 256 + ch * 2));
     }
-#define KV(t) ((t) & 1 ? bf16_hi(kp[(t) / 2]) : bf16_lo(kp[(t) / 2]))
-#define QV(t) ((t) & 1 ? bf16_hi(qp[(t) / 2]) : bf16_lo(qp[(t) / 2]))
+#define KV(u) ((u) & 1 ? bf16_hi(kp[(u) / 2]) : bf16_lo(kp[(u) / 2]))
+#define QV(u) ((u) & 1 ? bf16_hi(qp[(u) / 2]) : bf16_lo(qp[(u) / 2]))
+    __syncthreads();  // sTot / sQf visible
+    const float P0 = sTot[0][ch], P1 = sTot[1][ch];
     {
-        // prefix pass: (beta K o E)^T to smem, scale * (Q o E) and exp(G_last) to the record
-        float E = 1.f;
+        // prefix pass: (beta K o E)^T to smem, scale * (Q o E) to the record
+        float E = half ? P0 : 1.f;
 #pragma unroll
-        for (int tg = 0; tg < 8; ++tg) {
+        for (int tg = 0; tg < 4; ++tg) {
             float kb[8], qh[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int t = tg * 8 + u;
-                E *= al[t];
-                kb[u] = sBeta[t] * KV(t) * E;
-                qh[u] = P.scale * QV(t) * E;
+                const int uu = tg * 8 + u;
+                E *= al[uu];
+                kb[u] = sBeta[t0 + uu] * KV(uu) * E;
+                qh[u] = P.scale * QV(uu) * E;
             }
-            st_shared_v4(smem_addr(sm + kSmKbT + kmaj_off(ch, tg * 8, 128, 1024)),
-                         pack_bf16(kb[0], kb[1]), pack_bf16(kb[2], kb[3]), pack_bf16(kb[4], kb[5]),
-                         pack_bf16(kb[6], kb[7]));
-            stg_v4(rec + kRecWQ + mnmaj_off(64 + tg * 8, ch, 128, 2048), pack_bf16(qh[0], qh[1]),
-                   pack_bf16(qh[2], qh[3]), pack_bf16(qh[4], qh[5]), pack_bf16(qh[6], qh[7]));
+            sts_v4f(smem_addr(sm + kSmKbT + kmaj_off(ch, t0 + tg * 8, 128, 1024)), kb);
+            stg_v4f(rec + kRecWQ + mnmaj_off(64 + t0 + tg * 8, ch, 128, 2048), qh);
         }
-        reinterpret_cast<float*>(rec + kRecGam)[ch] = E;
+        if (half == 0) reinterpret_cast<float*>(rec + kRecGam)[ch] = P0 * P1;
         // suffix pass: (K o F)^T to the record
-        float F = 1.f;
+        float F = half ? 1.f : P1;
 #pragma unroll
-        for (int tg = 7; tg >= 0; --tg) {
+        for (int tg = 3; tg >= 0; --tg) {
             float kt[8];
 #pragma unroll
             for (int u = 7; u >= 0; --u) {
-                const int t = tg * 8 + u;
-                kt[u] = KV(t) * F;
-                F *= al[t];
+                const int uu = tg * 8 + u;
+                kt[u] = KV(uu) * F;
+                F *= al[uu];
             }
-            stg_v4(rec + kRecKT + kmaj_off(ch, tg * 8, 128, 1024), pack_bf16(kt[0], kt[1]),
-                   pack_bf16(kt[2], kt[3]), pack_bf16(kt[4], kt[5]), pack_bf16(kt[6], kt[7]));
+            stg_v4f(rec + kRecKT + kmaj_off(ch, t0 + tg * 8, 128, 1024), kt);
         }
         // (beta V)^T (thread = value channel)
 #pragma unroll
-        for (int tg = 0; tg < 8; ++tg) {
+        for (int tg = 0; tg < 4; ++tg) {
             float vb[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int t = tg * 8 + u;
+                const int t = t0 + tg * 8 + u;
                 vb[u] = sBeta[t] * lds_bf16(sm, kSmV + t * 256 + ch * 2);
             }
-            st_shared_v4(smem_addr(sm + kSmVbT + kmaj_off(ch, tg * 8, 128, 1024)),
-                         pack_bf16(vb[0], vb[1]), pack_bf16(vb[2], vb[3]), pack_bf16(vb[4], vb[5]),
-                         pack_bf16(vb[6], vb[7]));
+            sts_v4f(smem_addr(sm + kSmVbT + kmaj_off(ch, t0 + tg * 8, 128, 1024)), vb);
         }
     }
     __syncthreads();  // staging fully consumed; Left / R may now overwrite it
 
     // ---------------------------------------------------------------- score operands
+    {
+        // left factors exp(G_i - G_{m_a}) for this half's two sub-blocks
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        const int b0 = 16 * a;
-        // left factors exp(G_i - G_{m_a}) for the 16 tokens of sub-block a (m_a = b0 + 7)
-        float lf[16];
-        {
+        for (int bl = 0; bl < 2; ++bl) {
+            const int a = 2 * half + bl;  // global sub-block
+            const int u0 = 16 * bl;       // its first local token
+            float lf[16];
             float run = 1.f;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                run *= al[b0 + u];
-                lf[u] = run;  // prod_{s=b0}^{b0+u}
+                run *= al[u0 + u];
+                lf[u] = run;
             }
             const float inv = 1.f / lf[7];
 #pragma unroll
@@ -228,56 +290,67 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
             run = 1.f;
 #pragma unroll
             for (int u = 8; u < 16; ++u) {
-                run *= al[b0 + u];
-                lf[u] = run;  // prod_{s=m_a+1}^{b0+u}
+                run *= al[u0 + u];
+                lf[u] = run;
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float kl[8], ql[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    kl[u] = KV(u0 + hh * 8 + u) * lf[hh * 8 + u];
+                    ql[u] = QV(u0 + hh * 8 + u) * lf[hh * 8 + u];
+                }
+                sts_v4f(smem_addr(sm + kSmLeft + mnmaj_off(32 * a + 8 * hh, ch, 128, 2048)), kl);
+                sts_v4f(smem_addr(sm + kSmLeft + mnmaj_off(32 * a + 16 + 8 * hh, ch, 128, 2048)),
+                        ql);
             }
         }
-        // rows 32a .. 32a+15: k-left; 32a+16 .. 32a+31: q-left (MN-major, LBO 2048, SBO 128)
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float kl[8], ql[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int t = b0 + half * 8 + u;
-                kl[u] = KV(t) * lf[half * 8 + u];
-                ql[u] = QV(t) * lf[half * 8 + u];
-            }
-            st_shared_v4(smem_addr(sm + kSmLeft + mnmaj_off(32 * a + 8 * half, ch, 128, 2048)),
-                         pack_bf16(kl[0], kl[1]), pack_bf16(kl[2], kl[3]), pack_bf16(kl[4], kl[5]),
-                         pack_bf16(kl[6], kl[7]));
-            st_shared_v4(smem_addr(sm + kSmLeft + mnmaj_off(32 * a + 16 + 8 * half, ch, 128, 2048)),
-                         pack_bf16(ql[0], ql[1]), pack_bf16(ql[2], ql[3]), pack_bf16(ql[4], ql[5]),
-                         pack_bf16(ql[6], ql[7]));
-        }
-        // right operand R_a[j] = k_j o exp(G_{m_a} - G_j), j < 16(a+1)
-        float rf[64];
+        // right operands inside this half: R_{2h} rows [32h, 32h+16), R_{2h+1} rows [32h, 32h+32)
         {
-            const int m = b0 + 7;
-            rf[m] = 1.f;
-            float run = 1.f;
+            float rf0[16], rf1[32];
+            right_factors(al, rf0, rf1);
+            const int a0 = 2 * half, a1 = 2 * half + 1;
 #pragma unroll
-            for (int j = m - 1; j >= 0; --j) {
-                run *= al[j + 1];
-                rf[j] = run;  // prod_{s=j+1}^{m}
+            for (int jg = 0; jg < 2; ++jg) {
+                float r8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) r8[u] = KV(jg * 8 + u) * rf0[jg * 8 + u];
+                sts_v4f(smem_addr(sm + kSmR + r_off(a0) + mnmaj_off(t0 + jg * 8, ch, 128, 2048)),
+                        r8);
             }
-            run = 1.f;
 #pragma unroll
-            for (int j = b0 + 15; j > m; --j) {
-                rf[j] = run;  // prod_{s=j+1}^{b0+15}
-                run *= al[j];
+            for (int jg = 0; jg < 4; ++jg) {
+                float r8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) r8[u] = KV(jg * 8 + u) * rf1[jg * 8 + u];
+                sts_v4f(smem_addr(sm + kSmR + r_off(a1) + mnmaj_off(t0 + jg * 8, ch, 128, 2048)),
+                        r8);
             }
-            const float inv = 1.f / run;  // run = prod_{s=m+1}^{b0+15}
-#pragma unroll
-            for (int j = m + 1; j <= b0 + 15; ++j) rf[j] *= inv;
         }
+        if (half == 0) {
+            // R_2 and R_3 rows [0, 32): prod_{j+1}^{31} alpha (local) times the
+            // second half's prod_{32}^{m_a} alpha
+            const float q2 = sQf[0][ch], q3 = sQf[1][ch];
+            float run = 1.f;
+            float sfx[32];
 #pragma unroll
-        for (int jg = 0; jg < 2 * (a + 1); ++jg) {
-            float r8[8];
+            for (int u = 31; u >= 0; --u) {
+                sfx[u] = run;
+                run *= al[u];
+            }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) r8[u] = KV(jg * 8 + u) * rf[jg * 8 + u];
-            st_shared_v4(smem_addr(sm + kSmR + r_off(a) + mnmaj_off(jg * 8, ch, 128, 2048)),
-                         pack_bf16(r8[0], r8[1]), pack_bf16(r8[2], r8[3]), pack_bf16(r8[4], r8[5]),
-                         pack_bf16(r8[6], r8[7]));
+            for (int jg = 0; jg < 4; ++jg) {
+                float r2[8], r3[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float kv = KV(jg * 8 + u) * sfx[jg * 8 + u];
+                    r2[u] = kv * q2;
+                    r3[u] = kv * q3;
+                }
+                sts_v4f(smem_addr(sm + kSmR + r_off(2) + mnmaj_off(jg * 8, ch, 128, 2048)), r2);
+                sts_v4f(smem_addr(sm + kSmR + r_off(3) + mnmaj_off(jg * 8, ch, 128, 2048)), r3);
+            }
         }
     }
 #undef KV
@@ -310,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
     if (s_abort) goto teardown;
 
     // ---------------------------------------------------------------- score read-out
-    {
+    if (warp < 4) {
         const int a = warp;
         const bool is_k = lane < 16;
         const int i = 16 * a + (lane & 15);
@@ -322,11 +395,18 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
 #pragma unroll
             for (int u = 0; u < 16; ++u) row[16 * c + u] = __uint_as_float(r[u]);
         }
-        float* sA = reinterpret_cast<float*>(sm + kSmA);
         if (is_k) {
+            float* sA = reinterpret_cast<float*>(sm + kSmA);
             const float b = sBeta[i];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) sA[i * kAStride + j] = (j < i) ? b * row[j] : 0.f;
+            for (int j = 0; j < 64; j += 4) {
+                float4 x;
+                x.x = (j + 0 < i) ? b * row[j + 0] : 0.f;
+                x.y = (j + 1 < i) ? b * row[j + 1] : 0.f;
+                x.z = (j + 2 < i) ? b * row[j + 2] : 0.f;
+                x.w = (j + 3 < i) ? b * row[j + 3] : 0.f;
+                *reinterpret_cast<float4*>(sA + i * kStr + j) = x;
+            }
         } else {
 #pragma unroll
             for (int jg = 0; jg < 8; ++jg) {
@@ -338,45 +418,89 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
                     hi[u] = __bfloat162float(__float2bfloat16_rn(o));
                     lo[u] = o - hi[u];
                 }
-                stg_v4(rec + kRecAQ + kmaj_off(i, jg * 8, 128, 1024), pack_bf16(hi[0], hi[1]),
-                       pack_bf16(hi[2], hi[3]), pack_bf16(hi[4], hi[5]), pack_bf16(hi[6], hi[7]));
-                stg_v4(rec + kRecAQL + kmaj_off(i, jg * 8, 128, 1024), pack_bf16(lo[0], lo[1]),
-                       pack_bf16(lo[2], lo[3]), pack_bf16(lo[4], lo[5]), pack_bf16(lo[6], lo[7]));
+                stg_v4f(rec + kRecAQ + kmaj_off(i, jg * 8, 128, 1024), hi);
+                stg_v4f(rec + kRecAQL + kmaj_off(i, jg * 8, 128, 1024), lo);
             }
+        }
+    } else {
+        // zero the strictly upper 16 x 16 blocks of T
+        float* sT = reinterpret_cast<float*>(sm + kSmT);
+        for (int e = tid - 128; e < 6 * 256; e += 128) {
+            const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+            const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            sT[(16 * a + r) * kStr + 16 * b + c] = 0.f;
         }
     }
     tc_fence_before();
     __syncthreads();
 
     // ---------------------------------------------------------------- T = (I + A)^-1
-    if (tid < kChunk) {
-        const int j = tid;
+    {
         const float* sA = reinterpret_cast<const float*>(sm + kSmA);
-        float tcol[kChunk];
+        float* sT = reinterpret_cast<float*>(sm + kSmT);
+        float* sX = reinterpret_cast<float*>(sm + kSmX);
+        if (warp < 4 && lane < 16) {
+            // diagonal block `warp`, column `lane`, by forward substitution
+            const int o = 16 * warp, j = lane;
+            float tc[16];
 #pragma unroll
-        for (int l = 0; l < kChunk; ++l) tcol[l] = (l == j) ? 1.f : 0.f;
+            for (int l = 0; l < 16; ++l) tc[l] = (l == j) ? 1.f : 0.f;
 #pragma unroll
-        for (int i = 1; i < kChunk; ++i) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int i = 1; i < 16; ++i) {
+                float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int l = 0; l < i; l += 4) {
-                const float4 a4 = *reinterpret_cast<const float4*>(sA + i * kAStride + l);
-                acc[0] = fmaf(a4.x, tcol[l], acc[0]);
-                if (l + 1 < i) acc[1] = fmaf(a4.y, tcol[l + 1], acc[1]);
-                if (l + 2 < i) acc[2] = fmaf(a4.z, tcol[l + 2], acc[2]);
-                if (l + 3 < i) acc[3] = fmaf(a4.w, tcol[l + 3], acc[3]);
+                for (int l = 0; l < i; ++l) {
+                    if (l & 1)
+                        s1 = fmaf(sA[(o + i) * kStr + o + l], tc[l], s1);
+                    else
+                        s0 = fmaf(sA[(o + i) * kStr + o + l], tc[l], s0);
+                }
+                if (i > j) tc[i] = -(s0 + s1);
             }
-            const float s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-            tcol[i] = (i > j) ? -s : tcol[i];
-        }
-        // T^T as MN-major B operand: element (n = t, k = j), LBO 1024, SBO 128
 #pragma unroll
-        for (int tg = 0; tg < 8; ++tg)
-            st_shared_v4(smem_addr(sm + kSmTT + mnmaj_off(tg * 8, j, 128, 1024)),
-                         pack_bf16(tcol[tg * 8 + 0], tcol[tg * 8 + 1]),
-                         pack_bf16(tcol[tg * 8 + 2], tcol[tg * 8 + 3]),
-                         pack_bf16(tcol[tg * 8 + 4], tcol[tg * 8 + 5]),
-                         pack_bf16(tcol[tg * 8 + 6], tcol[tg * 8 + 7]));
+            for (int i = 0; i < 16; ++i) sT[(o + i) * kStr + o + j] = tc[i];
+        }
+        __syncthreads();
+        // off-diagonal blocks, one diagonal distance d at a time:
+        //   X_ab = sum_{c=b}^{a-1} A_ac T_cb ;  T_ab = -T_aa X_ab   (a = b + d)
+#pragma unroll
+        for (int d = 1; d < 4; ++d) {
+            const int nblk = 4 - d;
+            for (int e = tid; e < nblk * 256; e += kThreads) {
+                const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                const int a = b + d;
+                float s = 0.f;
+                for (int cb = b; cb < a; ++cb) {
+#pragma unroll
+                    for (int l = 0; l < 16; ++l)
+                        s = fmaf(sA[(16 * a + r) * kStr + 16 * cb + l],
+                                 sT[(16 * cb + l) * kStr + 16 * b + c], s);
+                }
+                sX[b * 256 + r * 16 + c] = s;
+            }
+            __syncthreads();
+            for (int e = tid; e < nblk * 256; e += kThreads) {
+                const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                const int a = b + d;
+                float s = 0.f;
+#pragma unroll
+                for (int l = 0; l < 16; ++l)
+                    s = fmaf(sT[(16 * a + r) * kStr + 16 * a + l], sX[b * 256 + l * 16 + c], s);
+                sT[(16 * a + r) * kStr + 16 * b + c] = -s;
+            }
+            __syncthreads();
+        }
+        // T^T as MN-major B operand: element (n = t, k = s), k-groups 128 B, n-groups 1024 B
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int e = tid + kThreads * it;   // 512 vectors: (t-group, s)
+            const int s = e & 63, tg = e >> 6;
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x[u] = sT[(tg * 8 + u) * kStr + s];
+            sts_v4f(smem_addr(sm + kSmTT + mnmaj_off(tg * 8, s, 128, 1024)), x);
+        }
     }
     fence_async_smem();
     tc_fence_before();
@@ -407,29 +531,24 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
     __syncthreads();
     if (s_abort) goto teardown;
 
-    // ---------------------------------------------------------------- W, U^T to the record
+    // ---------------------------------------------------------------- W (warps 0-3), U^T (4-7)
+    {
+        const bool is_w = warp < 4;
+        const uint32_t col0 = is_w ? 0u : 64u;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint32_t r[16];
-        tmem_load16(taddr(tbase, 32u * warp, 16u * c), r);  // W[16c + u][ch]
+        for (int c = 0; c < 4; ++c) {
+            uint32_t r[16];
+            tmem_load16(taddr(tbase, 32u * (warp & 3), col0 + 16u * c), r);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const uint32_t* x = r + 8 * half;
-            stg_v4(rec + kRecWQ + mnmaj_off(16 * c + 8 * half, ch, 128, 2048),
-                   pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
-                   pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
-                   pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
-                   pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
-        }
-        tmem_load16(taddr(tbase, 32u * warp, 64u + 16u * c), r);  // U[16c + u][ch]
+            for (int hh = 0; hh < 2; ++hh) {
+                float x[8];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const uint32_t* x = r + 8 * half;
-            stg_v4(rec + kRecUT + ch * 128 + (16 * c + 8 * half) * 2,
-                   pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
-                   pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
-                   pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
-                   pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
+                for (int u = 0; u < 8; ++u) x[u] = __uint_as_float(r[8 * hh + u]);
+                if (is_w)
+                    stg_v4f(rec + kRecWQ + mnmaj_off(16 * c + 8 * hh, ch, 128, 2048), x);
+                else
+                    stg_v4f(rec + kRecUT + ch * 128 + (16 * c + 8 * hh) * 2, x);
+            }
         }
     }
 
