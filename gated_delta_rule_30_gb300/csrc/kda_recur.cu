@@ -18,8 +18,12 @@
 //
 // Warp roles (192 threads): warps 0-3 own the 4 TMEM lane quarters (state
 // snapshot / decay, Delta for rows 0-63, output rows 64-127, state I/O); warp
-// 4 streams records with bulk copies into a 2-stage ring; warp 5 issues the
-// MMAs.  Every mbarrier wait is bounded; on timeout the CTA records
+// 4 streams records with bulk copies into a 2- or 3-stage ring (and prefetches
+// upcoming records into L2); warp 5 issues the
+// MMAs.  Only X = [W;Q].S, Delta and the state update are on the sequential
+// chain; the output update for chunk i has its own barrier and, with a
+// 3-stage ring, is issued after chunk i+1's first MMA (Delta is
+// double-buffered for that).  Every mbarrier wait is bounded; on timeout the CTA records
 // kStatusTimeout, stops, waits (bounded) for its own copies and frees TMEM.
 #include <cuda_runtime.h>
 
@@ -43,9 +47,11 @@ struct RecurLayout {
     static constexpr uint32_t kStageUT = kRecOperands;               // VS x 128 B
     static constexpr uint32_t kStageGam = kRecOperands + VS * 128;   // 512 B
     static constexpr uint32_t kStageBytes = kStageGam + 512;
-    static constexpr uint32_t kSb = 2 * kStageBytes;        // S snapshot, K=128 x N=VS, MN-major
-    static constexpr uint32_t kDb = kSb + VS * 256;         // Delta, K=64 x N=VS, MN-major
-    static constexpr uint32_t kBytes = kDb + VS * 128;
+    // ring depth: three stages when they fit next to the snapshot and Delta buffers
+    static constexpr int kStages = (3 * kStageBytes + VS * 256 + 2 * VS * 128 <= 232448) ? 3 : 2;
+    static constexpr uint32_t kSb = kStages * kStageBytes;  // S snapshot, K=128 x N=VS, MN-major
+    static constexpr uint32_t kDb = kSb + VS * 256;         // 2 x Delta, K=64 x N=VS, MN-major
+    static constexpr uint32_t kBytes = kDb + 2 * VS * 128;
     static constexpr uint32_t kLoadBytes = kRecOperands + VS * 128 + 512;
     static constexpr uint32_t kTmemCols = (3 * VS <= 128) ? 128 : (3 * VS <= 256 ? 256 : 512);
 };
@@ -114,13 +120,25 @@ struct StateIO<__nv_bfloat16> {
 };
 struct NoState {};
 
+// Bounded wait that records a timeout and raises the CTA's abort flag.
+#define WAIT_OR_ABORT(bar, parity)                         \
+    if (!mbar_wait((bar), (parity))) {                     \
+        atomicOr(P.status, kStatusTimeout);                \
+        s_abort = 1;                                       \
+        break;                                             \
+    }
+
 // H0 / HT: float, __nv_bfloat16 or NoState
 template <int VS, typename H0, typename HT>
 __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
     using L = RecurLayout<VS>;
     constexpr int kSlices = kDim / VS;
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t full[2], empty[2], s_ready, mma1, d_ready, mma2;
+    // full/empty: record ring; s_ready: snapshot written; mma1: X = [W;Q].S done;
+    // d_ready: Delta written; mma2s: state update done; mma2o: output update done
+    constexpr int NS = L::kStages;
+    __shared__ uint64_t full[NS], empty[NS], s_ready, mma1, d_ready, mma2s, mma2o;
+    __shared__ ChunkInfo sInfo[NS];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
@@ -143,14 +161,15 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
-        mbar_init(&empty[0], 1);
-        mbar_init(&empty[1], 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
         mbar_init(&s_ready, 128);
         mbar_init(&mma1, 1);
         mbar_init(&d_ready, 64);
-        mbar_init(&mma2, 1);
+        mbar_init(&mma2s, 1);
+        mbar_init(&mma2o, 1);
         mbar_fence_init();
         s_abort = 0;
     }
@@ -158,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_base;
-    const uint32_t tS = tbase;  // columns [0, VS)
+    const uint32_t tS = tbase;  // columns [0, VS); X[b] at [VS (1 + b), VS (2 + b))
     const size_t state_base = ((size_t)n * H + h) * kDim * kDim;
 
     // initial state -> TMEM (thread = key channel)
@@ -184,17 +203,23 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
     if (warp == 4) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int fills[2] = {0, 0};
+            int fills[NS];
+            for (int s = 0; s < NS; ++s) fills[s] = 0;
+            constexpr int kAhead = NS + 2;  // records pulled into L2 this many chunks ahead
+            for (int i = 0; i < kAhead && i < nchunks; ++i)
+                bulk_prefetch_l2(P.records + ((size_t)(c_begin + i) * H + h) * kRecBytes,
+                                 kRecBytes);
             for (int i = 0; i < nchunks; ++i) {
-                const int s = i & 1;
-                if (fills[s] > 0 && !mbar_wait(&empty[s], (uint32_t)((fills[s] - 1) & 1))) {
-                    atomicOr(P.status, kStatusTimeout);
-                    s_abort = 1;
-                    break;
-                }
+                const int s = i % NS;
+                if (fills[s] > 0) WAIT_OR_ABORT(&empty[s], (uint32_t)((fills[s] - 1) & 1));
                 if (*((volatile int*)&s_abort)) break;
+                if (i + kAhead < nchunks)
+                    bulk_prefetch_l2(
+                        P.records + ((size_t)(c_begin + i + kAhead) * H + h) * kRecBytes,
+                        kRecBytes);
                 uint8_t* st = sm + s * L::kStageBytes;
                 const uint8_t* rec = P.records + ((size_t)(c_begin + i) * H + h) * kRecBytes;
+                sInfo[s] = P.info[c_begin + i];  // published by the arrive below
                 mbar_arrive_expect_tx(&full[s], L::kLoadBytes);
                 bulk_g2s(st, rec, kRecOperands, &full[s]);
                 bulk_g2s(st + L::kStageUT, rec + kRecUT + v0 * 128, VS * 128, &full[s]);
@@ -202,69 +227,95 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
                 ++fills[s];
             }
             // drain: every issued fill must have landed before the CTA exits
-            for (int s = 0; s < 2; ++s)
+            for (int s = 0; s < NS; ++s)
                 if (fills[s] > 0 && !mbar_wait(&full[s], (uint32_t)((fills[s] - 1) & 1)))
                     atomicOr(P.status, kStatusTimeout);
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc1 = idesc_bf16_f32(128, VS, true, true);
-            const uint32_t idesc2 = idesc_bf16_f32(128, VS, false, true);
-            const uint32_t sb = smem_addr(sm + L::kSb);
-            const uint32_t db = smem_addr(sm + L::kDb);
-            for (int i = 0; i < nchunks; ++i) {
-                const int s = i & 1;
-                const uint32_t ph = (uint32_t)(i & 1);
-                const uint32_t tX = tbase + VS * (1 + (i & 1));
-                const uint32_t st = smem_addr(sm + s * L::kStageBytes);
-                if (!mbar_wait(&full[s], (uint32_t)((i >> 1) & 1)) || !mbar_wait(&s_ready, ph)) {
-                    atomicOr(P.status, kStatusTimeout);
-                    s_abort = 1;
-                    break;
-                }
-                tc_fence_after();
+        // The whole warp runs the loop (descriptors stay warp-uniform); one
+        // elected lane issues.  Per chunk i the critical chain is
+        //   MMA1(i): X = [W;Q].S  ->  (Delta)  ->  MMA2s(i): S += Kt^T.Delta
+        // and the output update MMA2o(i): X[64:] += Aqk.Delta (hi and lo) has
+        // its own barrier, so the next snapshot never waits for it.
+        const uint32_t idesc1 = idesc_bf16_f32(128, VS, true, true);
+        const uint32_t idesc2 = idesc_bf16_f32(128, VS, false, true);
+        // Descriptors of stage 0 / Delta buffer 0; the other stage (buffer) is
+        // the same descriptor with its start-address field (bytes >> 4) moved by
+        // the stage (buffer) size, and one K=16 step moves it by 256 B (16).
+        const uint64_t dSb = smem_desc(smem_addr(sm + L::kSb), 128, 2048);
+        const uint64_t dDb0 = smem_desc(smem_addr(sm + L::kDb), 128, 1024);
+        const uint32_t st0 = smem_addr(sm);
+        const uint64_t dWQ0 = smem_desc(st0 + L::kStageWQ, 128, 2048);
+        const uint64_t dKT0 = smem_desc(st0 + L::kStageKT, 128, 1024);
+        // [* ; Aqk] operands: rows 0..63 start 8 KB before the data and only
+        // feed X rows 0..63, which are dead once Delta is formed
+        const uint64_t dAQ0 = smem_desc(st0 + L::kStageAQ - 8192, 128, 1024);
+        const uint64_t dAQL0 = smem_desc(st0 + L::kStageAQL - 8192, 128, 1024);
+        constexpr uint64_t kStageStep = L::kStageBytes >> 4;
+        // With three stages the output update of chunk i waits until after
+        // MMA1(i+1); with two, deferring it would release the stage too late
+        // for the next record copy, so it follows the state update directly.
+        constexpr bool kDeferOut = NS >= 3;
+        constexpr uint64_t kDbStep = (VS * 128) >> 4;
+        auto issue_out = [&](int j) {  // MMA2o(j)
+            const uint64_t so = (uint64_t)(j % NS) * kStageStep;
+            const uint64_t dd = dDb0 + (uint64_t)(j & 1) * kDbStep;
+            const uint32_t tXj = tbase + VS * (1 + (j & 1));
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tXj, dAQ0 + so + 16u * kk, dd + 16u * kk, idesc2, 1u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tXj, dAQL0 + so + 16u * kk, dd + 16u * kk, idesc2, 1u);
+                mma_commit(&mma2o);
+                mma_commit(&empty[j % NS]);
+            }
+            __syncwarp();
+        };
+        int i = 0;
+        for (; i < nchunks; ++i) {
+            const int s = i % NS;
+            const uint32_t ph = (uint32_t)(i & 1);
+            const uint32_t tX = tbase + VS * (1 + (i & 1));
+            WAIT_OR_ABORT(&full[s], (uint32_t)((i / NS) & 1));
+            WAIT_OR_ABORT(&s_ready, ph);
+            tc_fence_after();
+            const uint64_t so = (uint64_t)s * kStageStep;
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tX, smem_desc(st + L::kStageWQ + kk * 256, 128, 2048),
-                             smem_desc(sb + kk * 256, 128, 2048), idesc1, kk > 0 ? 1u : 0u);
+                    mma_bf16(tX, dWQ0 + so + 16u * kk, dSb + 16u * kk, idesc1, kk > 0 ? 1u : 0u);
                 mma_commit(&mma1);
-                if (!mbar_wait(&d_ready, ph)) {
-                    atomicOr(P.status, kStatusTimeout);
-                    s_abort = 1;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tS, smem_desc(st + L::kStageKT + kk * 256, 128, 1024),
-                             smem_desc(db + kk * 256, 128, 1024), idesc2, 1u);
-                // [* ; Aqk_hi] and [* ; Aqk_lo]: rows 0..63 start 8 KB before the
-                // data and only touch X rows 0..63, which are dead once Delta is formed
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tX, smem_desc(st + L::kStageAQ - 8192 + kk * 256, 128, 1024),
-                             smem_desc(db + kk * 256, 128, 1024), idesc2, 1u);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tX, smem_desc(st + L::kStageAQL - 8192 + kk * 256, 128, 1024),
-                             smem_desc(db + kk * 256, 128, 1024), idesc2, 1u);
-                mma_commit(&mma2);
-                mma_commit(&empty[s]);
             }
+            __syncwarp();
+            if (kDeferOut && i > 0) issue_out(i - 1);
+            WAIT_OR_ABORT(&d_ready, ph);
+            tc_fence_after();
+            const uint64_t dd = dDb0 + (uint64_t)(i & 1) * kDbStep;
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tS, dKT0 + so + 16u * kk, dd + 16u * kk, idesc2, 1u);
+                mma_commit(&mma2s);
+            }
+            __syncwarp();
+            if (!kDeferOut) issue_out(i);
         }
+        if (kDeferOut && i == nchunks && nchunks > 0) issue_out(nchunks - 1);
     } else {
         // ------------------------------------------------------------ state / epilogue warps
         const int row = tid;  // TMEM lane: key channel for S, token row for X
         int prev_tok0 = 0, prev_len = 0;
-        auto store_output = [&](int i_prev) {
-            // rows 64..127 of X[i_prev & 1] hold the outputs of chunk i_prev
+        auto store_output = [&](int j) {
+            // rows 64..127 of X[j & 1] hold the outputs of chunk j
             const int t = row - 64;
-            const uint32_t tX = tbase + VS * (1 + (i_prev & 1));
+            const uint32_t tXj = tbase + VS * (1 + (j & 1));
 #pragma unroll
             for (int c0 = 0; c0 < VS; c0 += 16) {
                 uint32_t r[16];
-                tmem_load16(taddr(tX, 32u * warp, (uint32_t)c0), r);
+                tmem_load16(taddr(tXj, 32u * warp, (uint32_t)c0), r);
                 if (t < prev_len) {
                     uint4* dst = reinterpret_cast<uint4*>(
                         reinterpret_cast<__nv_bfloat16*>(P.out) +
@@ -280,15 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
                 }
             }
         };
-        for (int i = 0; i < nchunks; ++i) {
-            const int s = i & 1;
+        int i = 0;
+        for (; i < nchunks; ++i) {
+            const int s = i % NS;
             const uint32_t ph = (uint32_t)(i & 1);
             const uint8_t* st = sm + s * L::kStageBytes;
-            if (!mbar_wait(&full[s], (uint32_t)((i >> 1) & 1))) {
-                atomicOr(P.status, kStatusTimeout);
-                s_abort = 1;
-                break;
-            }
+            WAIT_OR_ABORT(&full[s], (uint32_t)((i / NS) & 1));
+            const ChunkInfo ci = sInfo[s];
             // snapshot S (bf16, MN-major B operand K=128 x N=VS) and decay it in TMEM
             {
                 const float gam = reinterpret_cast<const float*>(st + L::kStageGam)[row];
@@ -316,29 +365,35 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
                 mbar_arrive(&s_ready);
             }
             if (warp >= 2) {
-                if (i > 0) store_output(i - 1);
-            } else {
-                // Delta = U - X[0:64] for token row `row`
-                if (!mbar_wait(&mma1, ph)) {
-                    atomicOr(P.status, kStatusTimeout);
-                    s_abort = 1;
-                    break;
+                if (i > 0) {
+                    WAIT_OR_ABORT(&mma2o, (uint32_t)((i - 1) & 1));
+                    tc_fence_after();
+                    store_output(i - 1);
                 }
+            } else {
+                // Delta = U - X[0:64] for token row `row`, into Db[i & 1]
+                const uint16_t* ut = reinterpret_cast<const uint16_t*>(st + L::kStageUT);
+                uint32_t u_pk[VS / 2];  // U[row][c], two bf16 per register, read before waiting
+#pragma unroll
+                for (int c = 0; c < VS; c += 2)
+                    u_pk[c / 2] = (uint32_t)ut[c * 64 + row] | ((uint32_t)ut[(c + 1) * 64 + row] << 16);
+                WAIT_OR_ABORT(&mma1, ph);
                 tc_fence_after();
                 const uint32_t tX = tbase + VS * (1 + (i & 1));
-                const uint16_t* ut = reinterpret_cast<const uint16_t*>(st + L::kStageUT);
+                uint8_t* db = sm + L::kDb + (i & 1) * (VS * 128);
 #pragma unroll
                 for (int c0 = 0; c0 < VS; c0 += 16) {
                     uint32_t r[16];
                     tmem_load16(taddr(tX, 32u * warp, (uint32_t)c0), r);
                     float d[16];
 #pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        d[u] = bf16_to_f(ut[(c0 + u) * 64 + row]) - __uint_as_float(r[u]);
+                    for (int u = 0; u < 16; ++u) {
+                        const uint32_t pk = u_pk[(c0 + u) / 2];
+                        d[u] = ((u & 1) ? bf16_hi(pk) : bf16_lo(pk)) - __uint_as_float(r[u]);
+                    }
 #pragma unroll
                     for (int half = 0; half < 2; ++half)
-                        st_shared_v4(smem_addr(sm + L::kDb +
-                                               mnmaj_off(c0 + 8 * half, row, 128, 1024)),
+                        st_shared_v4(smem_addr(db + mnmaj_off(c0 + 8 * half, row, 128, 1024)),
                                      pack_bf16(d[8 * half + 0], d[8 * half + 1]),
                                      pack_bf16(d[8 * half + 2], d[8 * half + 3]),
                                      pack_bf16(d[8 * half + 4], d[8 * half + 5]),
@@ -348,18 +403,20 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
                 tc_fence_before();
                 mbar_arrive(&d_ready);
             }
-            if (!mbar_wait(&mma2, ph)) {
-                atomicOr(P.status, kStatusTimeout);
-                s_abort = 1;
-                break;
-            }
+            WAIT_OR_ABORT(&mma2s, ph);
             tc_fence_after();
-            const ChunkInfo ci = P.info[c_begin + i];
             prev_tok0 = ci.tok0;
             prev_len = ci.len;
         }
         if (!*((volatile int*)&s_abort)) {
-            if (warp >= 2 && nchunks > 0) store_output(nchunks - 1);
+            if (warp >= 2 && nchunks > 0) {
+                if (mbar_wait(&mma2o, (uint32_t)((nchunks - 1) & 1))) {
+                    tc_fence_after();
+                    store_output(nchunks - 1);
+                } else {
+                    atomicOr(P.status, kStatusTimeout);
+                }
+            }
             if constexpr (!std::is_same<HT, NoState>::value) {
                 const int ch = row;
 #pragma unroll
