@@ -51,7 +51,7 @@ constexpr uint32_t kSmKbT = 90112;    // 16 KB   (beta K o E)^T
 constexpr uint32_t kSmBytes = 106496;
 // after the score MMAs (alias Left / R)
 constexpr int kStr = 68;              // fp32 row stride of the 64 x 64 tiles
-constexpr uint32_t kSmA = 0;          // A (beta-scaled, strictly lower), fp32 [64][kStr]
+constexpr uint32_t kSmA = 0;          // A^T (beta-scaled, strictly lower A), fp32 [64][kStr]
 constexpr uint32_t kSmT = 17408;      // T, fp32 [64][kStr]
 constexpr uint32_t kSmX = 34816;      // level products, fp32 [3][16][16]
 constexpr uint32_t kSmTT = 40960;     // T^T as MN-major B operand, bf16 8 KB
@@ -195,17 +195,20 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
     // ---------------------------------------------------------------- gate (32 tokens)
     float al[32];
     {
-        const float dtb = P.dt_bias[h * kDim + ch];
+        // In base 2: x2 = (g + dt_bias) log2(e); softplus(x) log2(e) = max(x2, 0) +
+        // log2(1 + 2^-|x2|); log2(alpha) = max(-exp(A_log) * that, lower_bound log2(e)).
+        constexpr float kLog2e = 1.4426950408889634f;
+        const float dtb2 = P.dt_bias[h * kDim + ch] * kLog2e;
         const float negA = -__expf(P.A_log[h]);
-        const float lb = P.lower_bound;
+        const float lb2 = P.lower_bound * kLog2e;
         float prod = 1.f;
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
             const int t = t0 + u;
-            const float x = lds_bf16(sm, kSmG + t * 256 + ch * 2) + dtb;
-            const float sp = fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
-            const float la = fmaxf(negA * sp, lb);
-            al[u] = (t < len) ? __expf(la) : 1.f;
+            const float x2 = fmaf(lds_bf16(sm, kSmG + t * 256 + ch * 2), kLog2e, dtb2);
+            const float sp2 = fmaxf(x2, 0.f) + hw_log2(1.f + hw_exp2(-fabsf(x2)));
+            const float a = hw_exp2(fmaxf(negA * sp2, lb2));
+            al[u] = (t < len) ? a : 1.f;
             prod *= al[u];
             if (half == 1 && u == 7) sQf[0][ch] = prod;   // prod_{32}^{39}
             if (half == 1 && u == 23) sQf[1][ch] = prod;  // prod_{32}^{55}
@@ -396,17 +399,11 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
             for (int u = 0; u < 16; ++u) row[16 * c + u] = __uint_as_float(r[u]);
         }
         if (is_k) {
-            float* sA = reinterpret_cast<float*>(sm + kSmA);
+            // A^T[j][i] = beta_i A[i][j] (column-major A: the inverse reads columns)
+            float* sAT = reinterpret_cast<float*>(sm + kSmA);
             const float b = sBeta[i];
 #pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-                float4 x;
-                x.x = (j + 0 < i) ? b * row[j + 0] : 0.f;
-                x.y = (j + 1 < i) ? b * row[j + 1] : 0.f;
-                x.z = (j + 2 < i) ? b * row[j + 2] : 0.f;
-                x.w = (j + 3 < i) ? b * row[j + 3] : 0.f;
-                *reinterpret_cast<float4*>(sA + i * kStr + j) = x;
-            }
+            for (int j = 0; j < 64; ++j) sAT[j * kStr + i] = (j < i) ? b * row[j] : 0.f;
         } else {
 #pragma unroll
             for (int jg = 0; jg < 8; ++jg) {
@@ -437,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
 
     // ---------------------------------------------------------------- T = (I + A)^-1
     {
-        const float* sA = reinterpret_cast<const float*>(sm + kSmA);
+        const float* sAT = reinterpret_cast<const float*>(sm + kSmA);  // sAT[l][i] = A[i][l]
         float* sT = reinterpret_cast<float*>(sm + kSmT);
         float* sX = reinterpret_cast<float*>(sm + kSmX);
         if (warp < 4 && lane < 16) {
@@ -452,9 +449,9 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
 #pragma unroll
                 for (int l = 0; l < i; ++l) {
                     if (l & 1)
-                        s1 = fmaf(sA[(o + i) * kStr + o + l], tc[l], s1);
+                        s1 = fmaf(sAT[(o + l) * kStr + o + i], tc[l], s1);
                     else
-                        s0 = fmaf(sA[(o + i) * kStr + o + l], tc[l], s0);
+                        s0 = fmaf(sAT[(o + l) * kStr + o + i], tc[l], s0);
                 }
                 if (i > j) tc[i] = -(s0 + s1);
             }
@@ -464,30 +461,44 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
         __syncthreads();
         // off-diagonal blocks, one diagonal distance d at a time:
         //   X_ab = sum_{c=b}^{a-1} A_ac T_cb ;  T_ab = -T_aa X_ab   (a = b + d)
+        // each thread computes a 2 x 2 tile (rows r, r+1; columns c, c+1)
 #pragma unroll
         for (int d = 1; d < 4; ++d) {
-            const int nblk = 4 - d;
-            for (int e = tid; e < nblk * 256; e += kThreads) {
-                const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            const int nitems = (4 - d) * 64;
+            if (tid < nitems) {
+                const int b = tid >> 6, r = ((tid >> 3) & 7) * 2, c = (tid & 7) * 2;
                 const int a = b + d;
-                float s = 0.f;
-                for (int cb = b; cb < a; ++cb) {
-#pragma unroll
-                    for (int l = 0; l < 16; ++l)
-                        s = fmaf(sA[(16 * a + r) * kStr + 16 * cb + l],
-                                 sT[(16 * cb + l) * kStr + 16 * b + c], s);
+                float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+                for (int l = 16 * b; l < 16 * a; ++l) {
+                    const float2 av = *reinterpret_cast<const float2*>(sAT + l * kStr + 16 * a + r);
+                    const float2 tv = *reinterpret_cast<const float2*>(sT + l * kStr + 16 * b + c);
+                    x00 = fmaf(av.x, tv.x, x00);
+                    x01 = fmaf(av.x, tv.y, x01);
+                    x10 = fmaf(av.y, tv.x, x10);
+                    x11 = fmaf(av.y, tv.y, x11);
                 }
-                sX[b * 256 + r * 16 + c] = s;
+                *reinterpret_cast<float2*>(sX + b * 256 + r * 16 + c) = make_float2(x00, x01);
+                *reinterpret_cast<float2*>(sX + b * 256 + (r + 1) * 16 + c) = make_float2(x10, x11);
             }
             __syncthreads();
-            for (int e = tid; e < nblk * 256; e += kThreads) {
-                const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            if (tid < nitems) {
+                const int b = tid >> 6, r = ((tid >> 3) & 7) * 2, c = (tid & 7) * 2;
                 const int a = b + d;
-                float s = 0.f;
+                float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
 #pragma unroll
-                for (int l = 0; l < 16; ++l)
-                    s = fmaf(sT[(16 * a + r) * kStr + 16 * a + l], sX[b * 256 + l * 16 + c], s);
-                sT[(16 * a + r) * kStr + 16 * b + c] = -s;
+                for (int l = 0; l < 16; ++l) {
+                    const float t0v = sT[(16 * a + r) * kStr + 16 * a + l];
+                    const float t1v = sT[(16 * a + r + 1) * kStr + 16 * a + l];
+                    const float2 xv = *reinterpret_cast<const float2*>(sX + b * 256 + l * 16 + c);
+                    y00 = fmaf(t0v, xv.x, y00);
+                    y01 = fmaf(t0v, xv.y, y01);
+                    y10 = fmaf(t1v, xv.x, y10);
+                    y11 = fmaf(t1v, xv.y, y11);
+                }
+                *reinterpret_cast<float2*>(sT + (16 * a + r) * kStr + 16 * b + c) =
+                    make_float2(-y00, -y01);
+                *reinterpret_cast<float2*>(sT + (16 * a + r + 1) * kStr + 16 * b + c) =
+                    make_float2(-y10, -y11);
             }
             __syncthreads();
         }
