@@ -69,6 +69,24 @@ def counted_work(p):
     return head_tokens, flops, head_tokens * BYTES_PER_HEAD_TOKEN + state_bytes
 
 
+def workload_config(w, p, alg_bytes, head_tokens, flops, world):
+    return {"workload": w.name, "B": p["B"], "T": p["T"], "H": p["H"], "K": D, "V": D,
+            "seed": w.seed, "state_dtype": str(p["state_dtype"]).replace("torch.", ""),
+            "parallelism": "replicas" if world > 1 else "single-gpu",
+            "l2": "inputs larger than L2 (%.2f GB per step vs 129 MB)" % (alg_bytes / 1e9),
+            "head_tokens_per_step": head_tokens, "counted_flop_per_step": flops,
+            "counted_bytes_per_step": alg_bytes}
+
+
+def kernel_source_hash(src):
+    """Hash of a kernel's source and the headers it includes (ties ncu counters to a build)."""
+    h = hashlib.sha256()
+    for name in (src, "tc.cuh", "kda_internal.h"):
+        with open(os.path.join(ROOT, "gated_delta_rule_30_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -208,10 +226,11 @@ def main():
                 rates.append(r["value"])
         val = statistics.median(rates)
         res = r
+        head_tokens, flops, alg_bytes = counted_work(p)
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1,
                 "steps": args.steps, "warmup": warmup, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": w.name},
+                "config": workload_config(w, p, alg_bytes, head_tokens, flops, 1),
                 "cpu_baseline": {"value": val, "unit": UNIT, "cores": res["cores"],
                                  "kind": "oracle", "sample": res["sample"]},
                 "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -330,11 +349,9 @@ def main():
     achieved = alg_bytes / (dom_ms * 1e-3) / 1e9
     roofline_s = max(flops / (bf16_peak * 1e12), alg_bytes / (hbm_peak * 1e9))
     traffic = None
-    src = {"chunk": "kda_prep.cu", "recurrence": "kda_recur.cu"}[dominant]
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
-        with open(os.path.join(ROOT, "gated_delta_rule_30_gb300", "csrc", src), "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        h = kernel_source_hash({"chunk": "kda_prep.cu", "recurrence": "kda_recur.cu"}[dominant])
         with open(tpath) as f:
             tr = json.load(f).get(dominant, {})
         if tr.get("source_sha256_16") == h and tr.get("workload") == args.workload:
@@ -345,12 +362,7 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": p["B"], "T": p["T"], "H": p["H"], "K": D, "V": D,
-                   "seed": w.seed, "state_dtype": str(p["state_dtype"]).replace("torch.", ""),
-                   "parallelism": "replicas" if world > 1 else "single-gpu",
-                   "l2": "inputs larger than L2 (%.2f GB per step vs 129 MB)" % (alg_bytes / 1e9),
-                   "head_tokens_per_step": head_tokens, "counted_flop_per_step": flops,
-                   "counted_bytes_per_step": alg_bytes},
+        "config": workload_config(w, p, alg_bytes, head_tokens, flops, world),
         "tflops": flops / (ms_step * 1e-3) / 1e12,
         "roofline_fraction_step": roofline_s / (ms_step * 1e-3),
         "stage_ms": stage_avg,
