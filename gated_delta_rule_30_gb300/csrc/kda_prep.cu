@@ -26,9 +26,11 @@
 // Work split (256 threads): for the gate, the decays and the scaled operands
 // thread (c, h) owns key channel c = tid % 128 and the 32 tokens of half
 // h = tid / 128 of the chunk (products that cross the halves are exchanged
-// through shared memory).  The four score products (one per row sub-block:
-// M = 128 rows = the k and q rows of that sub-block, N = 16(a+1) key tokens,
-// K = 128 channels) and the two WY products (M = 128 channels, N = 64 tokens,
+// through shared memory).  The score products (M = 128 rows = the k and q
+// rows of the four sub-blocks, N = 16 + 32 + 48 + 64 = 160 columns holding
+// the four right operands side by side, K = 128 channels; the rows of
+// sub-block a only read the columns of its own right operand) and the two WY
+// products (M = 128 channels, N = 64 tokens,
 // K = 64 tokens) run on tcgen05 with fp32 accumulators in TMEM.  The
 // triangular inverse is blocked: the four 16 x 16 diagonal blocks by forward
 // substitution (one warp each), then the off-diagonal blocks level by level,
@@ -364,17 +366,16 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
 
     // ---------------------------------------------------------------- score MMAs
     if (tid == 0) {
+        // R_0..R_3 are contiguous with one 2048-B stride between 8-row groups and
+        // their TMEM columns d_col(a) follow the same order, so all four score
+        // blocks are one MMA with N = 16 + 32 + 48 + 64 = 160 (8 instructions).
         tc_fence_after();
-        const uint32_t left = smem_addr(sm + kSmLeft);
+        const uint64_t dl = smem_desc(smem_addr(sm + kSmLeft), 128, 2048);
+        const uint64_t dr = smem_desc(smem_addr(sm + kSmR), 128, 2048);
+        const uint32_t idesc = idesc_bf16_f32(128, 160, true, true);
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const uint32_t idesc = idesc_bf16_f32(128, 16 * (a + 1), true, true);
-            const uint32_t right = smem_addr(sm + kSmR + r_off(a));
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tbase + d_col(a), smem_desc(left + kk * 256, 128, 2048),
-                         smem_desc(right + kk * 256, 128, 2048), idesc, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16(tbase, dl + 16u * kk, dr + 16u * kk, idesc, kk > 0 ? 1u : 0u);
         mma_commit(&bar);
     }
     if (!mbar_wait(&bar, 0)) {
