@@ -19,7 +19,7 @@ import ctypes
 import os
 
 __all__ = ["fwd", "lib", "library_path", "workspace_size", "device_status", "KDAError",
-           "selftest_tcgen05"]
+           "selftest_tcgen05", "set_recurrence_kernel", "set_stage_events"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libkda.so")
@@ -68,6 +68,8 @@ def lib():
         L.kda_last_error_message.argtypes = []
         L.kda_abi_version.restype = ctypes.c_int
         L.kda_abi_version.argtypes = []
+        L.kda_set_recurrence_kernel.restype = ctypes.c_int
+        L.kda_set_recurrence_kernel.argtypes = [i32]
         L.kda_set_stage_events.restype = ctypes.c_int
         L.kda_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         L.kda_selftest_tcgen05.restype = ctypes.c_int
@@ -206,6 +208,16 @@ def device_status(device=None):
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     with torch.cuda.device(dev):
         _check(lib().kda_device_status(_stream_ptr(dev)))
+
+
+RECURRENCE_KERNELS = {"auto": 0, "sliced": 1, "transposed": 2}
+
+
+def set_recurrence_kernel(kind: str = "auto"):
+    """Choose the recurrence kernel for later calls: "auto", "sliced" or "transposed"."""
+    if kind not in RECURRENCE_KERNELS:
+        raise ValueError(f"kind must be one of {sorted(RECURRENCE_KERNELS)}")
+    _check(lib().kda_set_recurrence_kernel(RECURRENCE_KERNELS[kind]))
 
 
 def set_stage_events(events):

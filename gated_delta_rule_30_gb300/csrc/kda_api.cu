@@ -254,6 +254,7 @@ kda_status_t build_problem(Problem& p, const void* q, const void* k, const void*
 
 cudaEvent_t g_stage_events[4] = {nullptr, nullptr, nullptr, nullptr};
 bool g_stage_on = false;
+int g_recur_kind = 0;  // kda_set_recurrence_kernel
 
 void stage_mark(int i, cudaStream_t st) {
     if (g_stage_on) cudaEventRecord(g_stage_events[i], st);
@@ -282,7 +283,7 @@ kda_status_t run(const Problem& p, void* workspace, size_t workspace_size, cudaS
     stage_mark(1, st);
     if (e == cudaSuccess) e = launch_prep(p, ws, status, st);
     stage_mark(2, st);
-    if (e == cudaSuccess) e = launch_recur(p, ws, status, st);
+    if (e == cudaSuccess) e = launch_recur(p, ws, status, st, g_recur_kind);
     stage_mark(3, st);
     kda_status_t rc = KDA_OK;
     if (e != cudaSuccess) rc = cuda_error(e, "kernel launch");
@@ -381,6 +382,13 @@ extern "C" const char* kda_status_string(kda_status_t s) {
 extern "C" const char* kda_last_error_message(void) { return kda::g_msg; }
 
 extern "C" int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+extern "C" kda_status_t kda_set_recurrence_kernel(int32_t kind) {
+    clear_error();
+    if (kind < 0 || kind > 2) return set_error(KDA_ERR_INVALID_ARGUMENT, "kind must be 0, 1 or 2");
+    g_recur_kind = kind;
+    return KDA_OK;
+}
 
 extern "C" kda_status_t kda_set_stage_events(void* const* events, int32_t count) {
     clear_error();

@@ -9,10 +9,11 @@
 //      unit-lower-triangular inverse, and the WY factors W, U on tcgen05.  It
 //      writes one fixed-size record per (chunk, head) whose operand tiles are
 //      already in the tcgen05 shared-memory layouts the next kernel uses.
-//   3. recurrence kernel (kda_recur.cu), one CTA per (sequence, head, value
-//      slice): keeps the fp32 state slice in TMEM, streams the records with
-//      bulk copies and runs the sequential chunk-to-chunk update and outputs
-//      on tcgen05.
+//   3. recurrence kernel, which keeps the fp32 state in TMEM, streams the
+//      records with bulk copies and runs the sequential chunk-to-chunk update
+//      and outputs on tcgen05: kda_recur.cu (one CTA per (sequence, head,
+//      value slice), for few pairs) or kda_recur_t.cu (one CTA per (sequence,
+//      head) with the state transposed, for many pairs).
 #pragma once
 #include <cstddef>
 #include <cstdint>
@@ -25,20 +26,21 @@ namespace kda {
 constexpr int kChunk = 64;  // tokens per chunk
 constexpr int kDim = 128;   // K = V = 128
 
-// Per-(chunk, head) record written by the chunk kernel (byte offsets).
-//   WQ : A operand [W ; scale*Qhat] of the state read-out, M = 128 rows (0..63 the
-//        W rows of the chunk's tokens, 64..127 the decayed queries), K = 128 key
-//        channels; MN-major, 8-row groups 2048 B apart, 8-channel groups 128 B apart.
-//   KT : A operand Ktilde^T of the state update, M = 128 key channels, K = 64
-//        tokens; K-major, 8-token groups 128 B apart, 8-channel groups 1024 B apart.
-//   AQ : scale*Aqk as an unevaluated bf16 sum hi + lo (lo = bf16(x - hi)),
-//        each the rows 64..127 of an M = 128, K = 64 token A operand; K-major,
-//        8-token groups 128 B apart, 8-row groups 1024 B apart.  Rows 0..63 of
-//        that operand are whatever lies
-//        in the 8 KB before it: they only feed accumulator rows that are dead.
+// Per-(chunk, head) record written by the chunk kernel (byte offsets), laid
+// out so that the recurrence kernel copies it whole and uses its pieces as
+// tcgen05 B operands in place:
+//   WQ : [scale*Qhat ; W], 128 rows (0..63 the decayed queries, 64..127 the W
+//        rows of the chunk's tokens) x 128 key channels; MN-major (rows
+//        contiguous inside a core matrix), 8-row groups 2048 B apart, 8-channel
+//        groups 128 B apart.  B operand of X^T = S^T . [Q ; W]^T (N = 128, K = 128).
+//   KT, AQ, AQL : 256 rows x 64 tokens, K-major (tokens contiguous inside a
+//        core matrix), 8-token groups 128 B apart, 8-row groups 1024 B apart:
+//        rows 0..127 = Ktilde^T (key channels), 128..191 = scale*Aqk as bf16
+//        hi, 192..255 = the bf16 lo remainder (lo = bf16(x - hi)).  B operand of
+//        the state and output update Delta^T . [Ktilde | Aqk_hi^T | Aqk_lo^T]
+//        (N = 256, K = 64).
 //   UT : U^T, [128 value channels][64 tokens] bf16 row-major.
 //   GAM: chunk-end decay exp(G_last) per key channel, fp32 [128].
-// The first kRecOperands bytes are copied verbatim into shared memory.
 constexpr uint32_t kRecWQ = 0;
 constexpr uint32_t kRecKT = 32768;
 constexpr uint32_t kRecAQ = 49152;    // hi
@@ -96,10 +98,16 @@ int* device_status_ptr();
 constexpr int kStatusDeviceInput = 1;
 constexpr int kStatusTimeout = 2;
 
-// Kernel launchers (kda_prep.cu, kda_recur.cu, kda_api.cu).
+// Kernel launchers (kda_prep.cu, kda_recur.cu, kda_recur_t.cu, kda_api.cu).
 cudaError_t launch_schedule(const Problem& p, const Workspace& ws, int* status, cudaStream_t st);
 cudaError_t launch_prep(const Problem& p, const Workspace& ws, int* status, cudaStream_t st);
-cudaError_t launch_recur(const Problem& p, const Workspace& ws, int* status, cudaStream_t st);
+// recurrence: kind 0 = chosen from the problem shape, 1 = value-sliced, 2 = transposed
+cudaError_t launch_recur(const Problem& p, const Workspace& ws, int* status, cudaStream_t st,
+                         int kind);
+cudaError_t launch_recur_sliced(const Problem& p, const Workspace& ws, int* status,
+                                cudaStream_t st);
+cudaError_t launch_recur_transposed(const Problem& p, const Workspace& ws, int* status,
+                                   cudaStream_t st);
 
 kda_status_t selftest_tcgen05(const void* a, const void* b, float* d, int N, int K,
                               cudaStream_t stream);

@@ -474,7 +474,8 @@ int recur_slice_width(const Problem& p, int num_sms) {
     return 32;
 }
 
-cudaError_t launch_recur(const Problem& p, const Workspace& ws, int* status, cudaStream_t st) {
+cudaError_t launch_recur_sliced(const Problem& p, const Workspace& ws, int* status,
+                                cudaStream_t st) {
     if (p.N == 0 || p.H == 0) return cudaSuccess;
     RecurArgs a;
     a.out = p.out;
@@ -495,6 +496,26 @@ cudaError_t launch_recur(const Problem& p, const Workspace& ws, int* status, cud
         case 64: return launch_recur_vs<64>(p, a, st);
         default: return launch_recur_vs<32>(p, a, st);
     }
+}
+
+bool recur_prefers_transposed(const Problem& p, int num_sms) {
+    // The transposed kernel runs one CTA per (sequence, head) and does a chunk
+    // in fewer, wider MMAs; measured on GB300 it is the faster one from about
+    // half a CTA per SM up (128 pairs x 32 chunks: 0.096 vs 0.111 ms), while
+    // 32 pairs x 1024 chunks take 2.0 ms transposed against 1.1 ms sliced.
+    return 2LL * p.N * p.H >= num_sms;
+}
+
+cudaError_t launch_recur(const Problem& p, const Workspace& ws, int* status, cudaStream_t st,
+                         int kind) {
+    if (kind == 0) {
+        int dev = 0, sms = 148;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        kind = recur_prefers_transposed(p, sms) ? 2 : 1;
+    }
+    return kind == 2 ? launch_recur_transposed(p, ws, status, st)
+                     : launch_recur_sliced(p, ws, status, st);
 }
 
 }  // namespace kda

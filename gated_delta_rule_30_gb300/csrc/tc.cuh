@@ -223,6 +223,16 @@ __device__ __forceinline__ bool elect_one() {
         : "=r"(is_leader));
     return is_leader != 0;
 }
+// D[tmem] (+)= A[tmem] * B[smem]: A is read from tensor memory (lane = row m,
+// 32-bit column c holds the two bf16 elements 2c (low half) and 2c+1 along K).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrive once on `bar` when every MMA issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(

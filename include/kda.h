@@ -174,6 +174,18 @@ int kda_abi_version(void);
 kda_status_t kda_set_stage_events(void* const* events, int32_t count);
 
 /*
+ * kda_set_recurrence_kernel -- selects the kernel that runs the sequential
+ * chunk-to-chunk recurrence (no counterpart on the pages; every choice computes
+ * the same operation to the same tolerance).  kind = 0 (default): chosen per
+ * call from the number of (sequence, head) pairs and the SM count; 1: the
+ * value-sliced kernel (state slices of 32..128 value channels, one CTA each);
+ * 2: the transposed kernel (one CTA per (sequence, head), state held as S^T).
+ * Process-wide, applies to later calls; not thread-safe.  Any other kind
+ * returns KDA_ERR_INVALID_ARGUMENT.
+ */
+kda_status_t kda_set_recurrence_kernel(int32_t kind);
+
+/*
  * kda_selftest_tcgen05 -- diagnostic for the tensor-core building blocks the
  * kernels use (no counterpart on the pages).  Runs one M=128 x N x K bf16 MMA
  * per operand-layout combination (A and B each K-major or MN-major, no

@@ -1,6 +1,7 @@
 """Parity of the CUDA path with the fp64 oracle (GPU).
 
-Every case draws seeded inputs with ``gated_delta_rule_30_gb300.inputs``,
+Every case runs once per recurrence kernel (value-sliced and transposed),
+draws seeded inputs with ``gated_delta_rule_30_gb300.inputs``,
 runs ``kda.fwd`` (through the C ABI) and compares the bf16 outputs and the
 final states with the oracle over the whole tensors: relative Frobenius error
 <= 5e-3 and max-abs error <= 3e-2.  Full-size workloads compare every output
@@ -16,6 +17,13 @@ from kda_testutil import (REC_BYTES, assert_close, decode_record, errors, read_s
                           run_oracle, to_dev)
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, params=["sliced", "transposed"])
+def recur_kernel(request, kda_lib):
+    kda_lib.set_recurrence_kernel(request.param)
+    yield request.param
+    kda_lib.set_recurrence_kernel("auto")
 
 
 def make(name, **kw):
@@ -185,6 +193,22 @@ def test_deterministic(kda_lib):
     o1, h1 = run_gpu(p)
     o2, h2 = run_gpu(p)
     assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_auto_choice_is_one_of_the_kernels(kda_lib, recur_kernel):
+    """Automatic selection runs one of the two kernels unchanged (bit-identical)."""
+    for name, kw in (("state_io", dict(n_seqs=700, H=1)), ("dense_prefill", dict(T=200, H=2)),
+                     ("state_io", dict(n_seqs=70, H=1))):
+        p = make(name, **kw)
+        o1, h1 = run_gpu(p)
+        kda_lib.set_recurrence_kernel("auto")
+        o2, h2 = run_gpu(p)
+        kda_lib.set_recurrence_kernel(recur_kernel)
+        pairs = p["N"] * p["H"]
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        chosen = "transposed" if 2 * pairs >= sms else "sliced"
+        if chosen == recur_kernel:
+            assert torch.equal(o1, o2) and torch.equal(h1, h2)
 
 
 def test_malformed_cu_seqlens_reported(kda_lib):
