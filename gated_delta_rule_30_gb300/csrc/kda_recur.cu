@@ -21,10 +21,12 @@
 // 4 streams records with bulk copies into a 2- or 3-stage ring (and prefetches
 // upcoming records into L2); warp 5 issues the
 // MMAs.  Only X = [W;Q].S, Delta and the state update are on the sequential
-// chain; the output update for chunk i has its own barrier and, with a
-// 3-stage ring, is issued after chunk i+1's first MMA (Delta is
-// double-buffered for that).  Every mbarrier wait is bounded; on timeout the CTA records
-// kStatusTimeout, stops, waits (bounded) for its own copies and frees TMEM.
+// chain; the output update for chunk i has its own barrier and is issued right
+// after the state update, so the tensor pipe (which runs a CTA's MMAs in issue
+// order) executes it while the next snapshot is taken and the record slot is
+// released a chunk earlier than if it followed the next first MMA.  Every
+// mbarrier wait is bounded; on timeout the CTA records kStatusTimeout, stops,
+// waits (bounded) for its own copies and frees TMEM.
 #include <cuda_runtime.h>
 
 #include <type_traits>
@@ -253,10 +255,6 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
         const uint64_t dAQ0 = smem_desc(st0 + L::kStageAQ - 8192, 128, 1024);
         const uint64_t dAQL0 = smem_desc(st0 + L::kStageAQL - 8192, 128, 1024);
         constexpr uint64_t kStageStep = L::kStageBytes >> 4;
-        // With three stages the output update of chunk i waits until after
-        // MMA1(i+1); with two, deferring it would release the stage too late
-        // for the next record copy, so it follows the state update directly.
-        constexpr bool kDeferOut = NS >= 3;
         constexpr uint64_t kDbStep = (VS * 128) >> 4;
         auto issue_out = [&](int j) {  // MMA2o(j)
             const uint64_t so = (uint64_t)(j % NS) * kStageStep;
@@ -290,7 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
                 mma_commit(&mma1);
             }
             __syncwarp();
-            if (kDeferOut && i > 0) issue_out(i - 1);
             WAIT_OR_ABORT(&d_ready, ph);
             tc_fence_after();
             const uint64_t dd = dDb0 + (uint64_t)(i & 1) * kDbStep;
@@ -301,9 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
                 mma_commit(&mma2s);
             }
             __syncwarp();
-            if (!kDeferOut) issue_out(i);
+            issue_out(i);
         }
-        if (kDeferOut && i == nchunks && nchunks > 0) issue_out(nchunks - 1);
     } else {
         // ------------------------------------------------------------ state / epilogue warps
         const int row = tid;  // TMEM lane: key channel for S, token row for X

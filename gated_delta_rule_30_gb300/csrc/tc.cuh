@@ -114,6 +114,15 @@ __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, boo
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
+// Close the calling thread's current group of cp.async copies.
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of the calling thread's committed groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // ----------------------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_async_smem() {
