@@ -23,6 +23,11 @@
 // Every exp(G_i - G_j) is a product of the alphas between i and j, so the
 // only transcendentals are those of the gate itself.
 //
+// The kernel is persistent (two CTAs per SM, each looping over (chunk, head)
+// items): once an item's last MMA has read shared memory, the copies of the
+// next item's q, k, v, g are issued, so they land while the current item's
+// results are written out.
+//
 // Work split (256 threads): for the gate, the decays and the scaled operands
 // thread (c, h) owns key channel c = tid % 128 and the 32 tokens of half
 // h = tid / 128 of the chunk (products that cross the halves are exchanged
@@ -150,49 +155,73 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
     // a CTA that already gave up on a bounded wait poisons the launch: skip the rest
     if (*((volatile int*)P.status) & kStatusTimeout) return;
     const int H = P.H;
-    const int chunk = blockIdx.x / H;
-    const int h = blockIdx.x - chunk * H;
-    if (chunk >= P.chunk_off[P.N]) return;
-    const ChunkInfo ci = P.info[chunk];
-    const int tok0 = ci.tok0, len = ci.len;
+    const int n_items = P.chunk_off[P.N] * H;  // valid (chunk, head) pairs
+    int item = blockIdx.x;
+    if (item >= n_items) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ch = tid & (kDim - 1);
     const int half = tid >> 7;
     const int t0 = 32 * half;  // first token of this thread's half
-    uint8_t* rec = P.records + ((size_t)chunk * H + h) * kRecBytes;
 
-    // ---------------------------------------------------------------- staging
-    {
-        const __nv_bfloat16* srcs[4] = {P.q, P.k, P.v, P.g};
+    // Issue the asynchronous copies of one item's q, k, v, g tiles (g in its
+    // own cp.async group, so the gate can start before q, k, v land) and set
+    // its beta.
+    auto stage = [&](const ChunkInfo& c, int hh, float beta_t) {
+        const __nv_bfloat16* srcs[4] = {P.g, P.q, P.k, P.v};
+        const uint32_t dsts[4] = {kSmG, kSmQ, kSmK, kSmV};
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
 #pragma unroll
             for (int it = 0; it < 4; ++it) {
-                const int c = tid + kThreads * it;
-                const int row = c >> 4, col = c & 15;
-                const bool ok = row < len;
+                const int e = tid + kThreads * it;
+                const int row = e >> 4, col = e & 15;
+                const bool ok = row < c.len;
                 const __nv_bfloat16* src =
-                    srcs[x] + ((size_t)(ok ? tok0 + row : tok0) * H + h) * kDim + col * 8;
-                cp_async16_zfill(sm + x * 16384 + row * 256 + col * 16, src, ok);
+                    srcs[x] + ((size_t)(ok ? c.tok0 + row : c.tok0) * H + hh) * kDim + col * 8;
+                cp_async16_zfill(sm + dsts[x] + row * 256 + col * 16, src, ok);
             }
+            if (x == 0) cp_async_commit();
         }
-        if (tid < kChunk)
-            sBeta[tid] = tid < len ? __bfloat162float(P.beta[(size_t)(tok0 + tid) * H + h]) : 0.f;
-        if (warp == 0) {
-            tmem_alloc(&tmem_base, kTmemCols);
-            tmem_relinquish();
-        }
-        if (tid == 0) {
-            mbar_init(&bar, 1);
-            mbar_fence_init();
-            s_abort = 0;
-        }
-        cp_async_wait_all();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        cp_async_commit();
+        if (tid < kChunk) sBeta[tid] = beta_t;
+    };
+    auto load_beta = [&](const ChunkInfo& c, int hh) -> float {
+        return (tid < c.len) ? __bfloat162float(P.beta[(size_t)(c.tok0 + tid) * H + hh]) : 0.f;
+    };
+
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, kTmemCols);
+        tmem_relinquish();
     }
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+        s_abort = 0;
+    }
+    int chunk = item / H;
+    int h = item - chunk * H;
+    ChunkInfo ci = P.info[chunk];
+    stage(ci, h, tid < kChunk ? load_beta(ci, h) : 0.f);
+    float dtb = P.dt_bias[h * kDim + ch];
+    float alog = P.A_log[h];
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     const uint32_t tbase = tmem_base;
+
+    for (;;) {
+    const int len = ci.len;
+    uint8_t* rec = P.records + ((size_t)chunk * H + h) * kRecBytes;
+    // the next item's chunk info and per-head parameters, loaded early
+    const int next = item + (int)gridDim.x;
+    const bool has_next = next < n_items;
+    const int chunk_n = has_next ? next / H : chunk;
+    const int h_n = has_next ? next - chunk_n * H : h;
+    const ChunkInfo ci_n = P.info[chunk_n];
+    const float dtb_n = P.dt_bias[h_n * kDim + ch];
+    const float alog_n = P.A_log[h_n];
+    cp_async_wait_group<1>();  // this thread's g copies
+    __syncthreads();
 
     // ---------------------------------------------------------------- gate (32 tokens)
     float al[32];
@@ -200,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
         // In base 2: x2 = (g + dt_bias) log2(e); softplus(x) log2(e) = max(x2, 0) +
         // log2(1 + 2^-|x2|); log2(alpha) = max(-exp(A_log) * that, lower_bound log2(e)).
         constexpr float kLog2e = 1.4426950408889634f;
-        const float dtb2 = P.dt_bias[h * kDim + ch] * kLog2e;
-        const float negA = -__expf(P.A_log[h]);
+        const float dtb2 = dtb * kLog2e;
+        const float negA = -__expf(alog);
         const float lb2 = P.lower_bound * kLog2e;
         float prod = 1.f;
 #pragma unroll
@@ -217,6 +246,8 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
         }
         sTot[half][ch] = prod;
     }
+    cp_async_wait_group<0>();  // q, k, v
+    __syncthreads();           // q, k, v, sTot, sQf visible
     uint32_t qp[16], kp[16];
 #pragma unroll
     for (int u = 0; u < 32; u += 2) {
@@ -228,7 +259,6 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
     }
 #define KV(u) ((u) & 1 ? bf16_hi(kp[(u) / 2]) : bf16_lo(kp[(u) / 2]))
 #define QV(u) ((u) & 1 ? bf16_hi(qp[(u) / 2]) : bf16_lo(qp[(u) / 2]))
-    __syncthreads();  // sTot / sQf visible
     const float P0 = sTot[0][ch], P1 = sTot[1][ch];
     {
         // prefix pass: (beta K o E)^T to smem, scale * (Q o E) to the record
@@ -306,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
                     kl[u] = KV(u0 + hh * 8 + u) * lf[hh * 8 + u];
                     ql[u] = QV(u0 + hh * 8 + u) * lf[hh * 8 + u];
                 }
-                sts_v4f(smem_addr(sm + kSmLeft + mnmaj_off(32 * a + 8 * hh, ch, 128, 2048)), kl);
-                sts_v4f(smem_addr(sm + kSmLeft + mnmaj_off(32 * a + 16 + 8 * hh, ch, 128, 2048)),
+                sts_v4f(smem_addr(sm + kSmLeft + mnmaj_off(16 * a + 8 * hh, ch, 128, 2048)), kl);
+                sts_v4f(smem_addr(sm + kSmLeft + mnmaj_off(64 + 16 * a + 8 * hh, ch, 128, 2048)),
                         ql);
             }
         }
@@ -384,46 +414,68 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
     }
     tc_fence_after();
     __syncthreads();
-    if (s_abort) goto teardown;
+    if (s_abort) break;
 
     // ---------------------------------------------------------------- score read-out
-    if (warp < 4) {
-        const int a = warp;
-        const bool is_k = lane < 16;
-        const int i = 16 * a + (lane & 15);
-        float row[64];
+    // TMEM lane quarter w % 4 holds k rows (quarters 0, 1) or q rows (2, 3) of
+    // tokens 32 (w % 2) .. + 31, i.e. sub-blocks a_lo = 2 (w % 2) (lanes 0-15)
+    // and a_lo + 1 (lanes 16-31); warps w and w + 4 split that row's columns j.
+    {
+        const int qd = warp & 3, hj = warp >> 2;
+        const bool is_k = qd < 2;
+        const int i = 32 * (qd & 1) + lane;  // token of this row
+        const int a_lo = 2 * (qd & 1);
+        const bool upper = lane >= 16;       // row of sub-block a_lo + 1
+        const int jw = (qd & 1) ? 32 : 16;   // columns per warp
+        float* sAT = reinterpret_cast<float*>(sm + kSmA);
+        const float f = is_k ? sBeta[i] : P.scale;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t r[16];
-            tmem_load16(taddr(tbase, 32u * a, d_col(a) + 16u * c), r);
+        for (int rr = 0; rr < 2; ++rr) {
+            if (rr * 16 >= jw) break;
+            const int jb = jw * hj + 16 * rr;
+            uint32_t r0[16], r1[16];
+            tmem_ld16(taddr(tbase, 32u * qd, d_col(a_lo) + (uint32_t)jb), r0);
+            tmem_ld16(taddr(tbase, 32u * qd, d_col(a_lo + 1) + (uint32_t)jb), r1);
+            tmem_wait_ld();
+            reg_fence16(r0);
+            reg_fence16(r1);
+            float val[16];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) row[16 * c + u] = __uint_as_float(r[u]);
-        }
-        if (is_k) {
-            // A^T[j][i] = beta_i A[i][j] (column-major A: the inverse reads columns)
-            float* sAT = reinterpret_cast<float*>(sm + kSmA);
-            const float b = sBeta[i];
+            for (int u = 0; u < 16; ++u) {
+                const int j = jb + u;
+                const float x = __uint_as_float(upper ? r1[u] : r0[u]);
+                val[u] = (is_k ? (j < i) : (j <= i)) ? f * x : 0.f;
+            }
+            if (is_k) {
+                // A^T[j][i] = beta_i A[i][j] (column-major A: the inverse reads columns)
 #pragma unroll
-            for (int j = 0; j < 64; ++j) sAT[j * kStr + i] = (j < i) ? b * row[j] : 0.f;
-        } else {
+                for (int u = 0; u < 16; ++u) sAT[(jb + u) * kStr + i] = val[u];
+            } else {
 #pragma unroll
-            for (int jg = 0; jg < 8; ++jg) {
-                float hi[8], lo[8];
+                for (int hh = 0; hh < 2; ++hh) {
+                    float hi[8], lo[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int j = jg * 8 + u;
-                    const float o = (j <= i) ? P.scale * row[j] : 0.f;
-                    hi[u] = __bfloat162float(__float2bfloat16_rn(o));
-                    lo[u] = o - hi[u];
+                    for (int u = 0; u < 8; ++u) {
+                        hi[u] = __bfloat162float(__float2bfloat16_rn(val[8 * hh + u]));
+                        lo[u] = val[8 * hh + u] - hi[u];
+                    }
+                    stg_v4f(rec + kRecAQ + kmaj_off(i, jb + 8 * hh, 128, 1024), hi);
+                    stg_v4f(rec + kRecAQL + kmaj_off(i, jb + 8 * hh, 128, 1024), lo);
                 }
-                stg_v4f(rec + kRecAQ + kmaj_off(i, jg * 8, 128, 1024), hi);
-                stg_v4f(rec + kRecAQL + kmaj_off(i, jg * 8, 128, 1024), lo);
             }
         }
-    } else {
+        if (qd == 2) {
+            // tokens 0..31 attend to no key in 32..63: zero those record columns
+#pragma unroll
+            for (int jg = 0; jg < 2; ++jg) {
+                const int j0 = 32 + 16 * hj + 8 * jg;
+                stg_v4(rec + kRecAQ + kmaj_off(i, j0, 128, 1024), 0u, 0u, 0u, 0u);
+                stg_v4(rec + kRecAQL + kmaj_off(i, j0, 128, 1024), 0u, 0u, 0u, 0u);
+            }
+        }
         // zero the strictly upper 16 x 16 blocks of T
         float* sT = reinterpret_cast<float*>(sm + kSmT);
-        for (int e = tid - 128; e < 6 * 256; e += 128) {
+        for (int e = tid; e < 6 * 256; e += kThreads) {
             const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
             const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
             const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
@@ -541,7 +593,12 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
     }
     tc_fence_after();
     __syncthreads();
-    if (s_abort) goto teardown;
+    if (s_abort) break;
+
+    // the staging area is free again: start the next item's copies
+    float beta_n = 0.f;
+    if (has_next && tid < kChunk) beta_n = load_beta(ci_n, h_n);
+    if (has_next) stage(ci_n, h_n, beta_n);
 
     // ---------------------------------------------------------------- W (warps 0-3), U^T (4-7)
     {
@@ -564,7 +621,17 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
         }
     }
 
-teardown:
+    if (!has_next) break;
+    item = next;
+    chunk = chunk_n;
+    h = h_n;
+    ci = ci_n;
+    dtb = dtb_n;
+    alog = alog_n;
+    tc_fence_before();
+    }  // item loop
+
+    cp_async_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
@@ -594,7 +661,12 @@ cudaError_t launch_prep(const Problem& p, const Workspace& ws, int* status, cuda
     a.info = ws.info;
     a.records = ws.records;
     a.status = status;
-    const long long blocks = (long long)p.max_chunks * p.H;
+    // persistent: two CTAs per SM, each looping over (chunk, head) items
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long items = (long long)p.max_chunks * p.H;
+    const long long blocks = items < 2LL * sms ? items : 2LL * sms;
     prep_kernel<<<(unsigned)blocks, kThreads, kSmBytes, st>>>(a);
     return cudaGetLastError();
 }
