@@ -7,30 +7,32 @@
 // The state is kept transposed, S^T (value channel v on the 128 TMEM lanes,
 // key channel k on 128 fp32 columns), so that the small, per-chunk matrices
 // are the tcgen05 A operands (read from TMEM) and the chunk record's wide
-// matrices are B operands read in place from shared memory.  Per chunk, with
+// matrices are B operands read in place from shared memory.  Per chunk i, with
 // the record written by the chunk kernel:
-//   X^T   = S^T . [W ; scale*Qhat]^T        (MMA1: A = bf16 S^T in TMEM, N = 128, K = 128)
+//   X^T   = S^T . [W ; scale*Qhat]^T        (MMA1: A = bf16 S^T in TMEM, N = 128, K = 128,
+//                                            into accumulator X[i % 2])
 //   Delta = U - X_W                         (v_new; bf16 Delta^T to TMEM)
-//   [S^T | X_W | X_Q] += Delta^T . [Ktilde | Aqk_hi^T | Aqk_lo^T]
-//                                           (MMA2: N = 256, K = 64; S^T was decayed
-//                                            by Diag(exp(G_last)) beforehand)
-//   O^T   = (X_Q + Aqk_lo Delta) + (X_W + Aqk_hi Delta) - X_W
-// (the two output halves share MMA2 with the state update; X_W is kept in
-// registers so that its column can take one of them)
-// which is the gated delta rule unrolled over the chunk (reading of
-// "Flashkda Delta Attention", "Core Kernel API": recurrent state updates of
-// delta attention).  A K=16 tcgen05 MMA costs a fixed ~44 cycles for N <= 64
-// on GB300, so two wide MMAs per chunk (8 + 4 instructions) replace the ~20
-// narrow ones a value-sliced formulation needs.
+//   S^T  += Delta^T . Ktilde                (MMA2s: N = 128, K = 64; S^T was decayed by
+//                                            Diag(exp(G_last)) beforehand)
+//   X_Q  += Delta^T . Aqk_hi^T + Delta^T . Aqk_lo^T   (MMA2o: N = 64, K = 64, twice)
+//   O^T   = X_Q
+// This is the gated delta rule unrolled over the chunk
+// (reading of "Flashkda Delta Attention", "Core Kernel API": recurrent state
+// updates of delta attention).  A K=16 tcgen05 MMA costs about 44 cycles for
+// N <= 64 on GB300 and 67 at N = 128, so wide MMAs on the chain (8 + 4
+// instructions per chunk) replace the ~12 narrow ones a value-sliced
+// formulation needs there.  Only MMA1, Delta and MMA2s are on the sequential
+// chain: MMA2o runs while the next snapshot is taken.
 //
-// Warp roles (320 threads): warps 0-7 are epilogue warps -- warp w owns TMEM
-// lane quarter w % 4 (32 value channels) and half w / 4 of the columns it
-// touches (state columns, or the chunk's tokens); warp 8 streams whole records
-// with one bulk copy each into a 2-stage ring; warp 9 issues the MMAs.  Outputs
-// leave TMEM before the next chunk's first MMA, are transposed through shared
-// memory and written as whole 256-byte token rows after that MMA is issued.  Every
-// mbarrier wait is bounded; on timeout the CTA records kStatusTimeout, stops,
-// drains its own copies and frees TMEM.
+// Warp roles (448 threads): warps 0-7 are chain warps -- warp w owns TMEM lane
+// quarter w % 4 (32 value channels) and half w / 4 of the columns it touches
+// (state columns, or the chunk's tokens) and takes the snapshot and Delta;
+// warp 8 streams whole records with one bulk copy each into a 2-stage ring;
+// warp 9 issues the MMAs; warps 10-13 (one per lane quarter) move the outputs
+// of chunk i out of X[i % 2] while later chunks run, transposing them through
+// shared memory into whole 256-byte token rows, and release X[i % 2] for
+// MMA1(i + 2).  Every mbarrier wait is bounded; on timeout the CTA records
+// kStatusTimeout, stops, drains its own copies and frees TMEM.
 #include <cuda_runtime.h>
 
 #include <type_traits>
@@ -42,17 +44,22 @@ namespace kda {
 namespace {
 
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (kEpiWarps + 2);
+constexpr int kOutWarps = 4;
+constexpr int kThreads = 32 * (kEpiWarps + 2 + kOutWarps);
+constexpr int kWarpProducer = kEpiWarps, kWarpMma = kEpiWarps + 1, kWarpOut0 = kEpiWarps + 2;
 constexpr int kStages = 2;
 constexpr uint32_t kStageBytes = kRecBytes;          // a whole record per stage
-constexpr uint32_t kSmemO = kStages * kStageBytes;   // output staging, bf16 [64 tokens][128 v]
-constexpr uint32_t kSmemBytes = kSmemO + kChunk * kDim * 2;
+constexpr uint32_t kTileO = kChunk * kDim * 2;       // output tile, bf16 [64 tokens][128 v]
+constexpr uint32_t kSmemO = kStages * kStageBytes;   // two output tiles
+constexpr uint32_t kSmemBytes = kSmemO + 2 * kTileO;
 // TMEM columns
 constexpr uint32_t kColS = 0;      // S^T, fp32, 128 columns
-constexpr uint32_t kColX = 128;    // [X_W | X_Q] (+ the output updates), 128 columns
+constexpr uint32_t kColX0 = 128;   // X[0] = [X_W | X_Q] (+ the output updates), 128 columns
 constexpr uint32_t kColSb = 256;   // bf16 S^T snapshot (A of MMA1), 64 columns
-constexpr uint32_t kColDb = 320;   // bf16 Delta^T (A of MMA2), 32 columns
+constexpr uint32_t kColDb = 320;   // bf16 Delta^T (A of MMA2s / MMA2o), 32 columns
+constexpr uint32_t kColX1 = 384;   // X[1]
 constexpr uint32_t kTmemCols = 512;
+__device__ __forceinline__ uint32_t col_x(int i) { return (i & 1) ? kColX1 : kColX0; }
 
 struct RecurTArgs {
     void* out;  // bf16 [tokens, H, 128]
@@ -102,10 +109,11 @@ __device__ __forceinline__ void tmem_st8(uint32_t ta, const uint32_t (&r)[8]) {
 template <typename H0, typename HT>
 __global__ void __launch_bounds__(kThreads, 1) recur_t_kernel(const RecurTArgs P) {
     extern __shared__ __align__(1024) uint8_t sm[];
-    // full/empty: record ring; s_ready: snapshot + previous outputs done;
-    // mma1: X^T ready; d_ready: Delta^T written; mma2: state / outputs updated
-    __shared__ uint64_t full[kStages], empty[kStages], s_ready, mma1, d_ready, mma2;
-    __shared__ ChunkInfo sInfo[kStages];
+    // full/empty: record ring; s_ready: snapshot written; mma1: X^T ready;
+    // d_ready: Delta^T written; mma2s: state updated; mma2o[b]: outputs of the
+    // chunk in X[b] complete; x_free[b]: the output warps have read X[b]
+    __shared__ uint64_t full[kStages], empty[kStages], s_ready, mma1, d_ready, mma2s, mma2o[2],
+        x_free[2];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
@@ -131,7 +139,11 @@ __global__ void __launch_bounds__(kThreads, 1) recur_t_kernel(const RecurTArgs P
         mbar_init(&s_ready, 32 * kEpiWarps);
         mbar_init(&mma1, 1);
         mbar_init(&d_ready, 32 * kEpiWarps);
-        mbar_init(&mma2, 1);
+        mbar_init(&mma2s, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&mma2o[b], 1);
+            mbar_init(&x_free[b], 32 * kOutWarps);
+        }
         mbar_fence_init();
         s_abort = 0;
     }
@@ -164,83 +176,51 @@ __global__ void __launch_bounds__(kThreads, 1) recur_t_kernel(const RecurTArgs P
         __syncthreads();
         tc_fence_after();
 
-        float xw[32];  // X_W of this thread's 32 tokens, kept for the chunk's outputs
-        int prev_tok0 = 0, prev_len = 0;
-        // outputs of the chunk whose MMA2 completed last, tokens [32 hc, 32 hc + 32):
-        // from TMEM into the shared staging tile O[t][v] (bf16)
-        __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(sm + kSmemO);
-        auto stage_output = [&]() {
-#pragma unroll
-            for (int c0 = 0; c0 < 32; c0 += 16) {
-                uint32_t a[16], b[16];
-                tmem_ld16(lane_base + kColX + 64 + 32 * hc + c0, a);  // X_Q + Aqk_lo Delta
-                tmem_ld16(lane_base + kColX + 32 * hc + c0, b);       // X_W + Aqk_hi Delta
-                tmem_wait_ld();
-                reg_fence16(a);
-                reg_fence16(b);
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int t = 32 * hc + c0 + u;
-                    const float o = __uint_as_float(a[u]) + (__uint_as_float(b[u]) - xw[c0 + u]);
-                    so[t * kDim + v] = __float2bfloat16_rn(o);
-                }
-            }
-        };
-        // staged outputs -> global, whole 256-byte token rows (epilogue warps only)
-        auto flush_output = [&]() {
-            asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
-#pragma unroll
-            for (int it = 0; it < (kChunk * kDim * 2 / 16) / (32 * kEpiWarps); ++it) {
-                const int e = tid + 32 * kEpiWarps * it;  // 16-byte piece
-                const int t = e >> 4, piece = e & 15;
-                if (t < prev_len)
-                    reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(P.out) +
-                                             ((size_t)(prev_tok0 + t) * H + h) * kDim)[piece] =
-                        reinterpret_cast<const uint4*>(so + t * kDim)[piece];
-            }
-            asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
-        };
         int i = 0;
         for (; i < nchunks; ++i) {
             const int s = i % kStages;
             const uint32_t ph = (uint32_t)(i & 1);
             const uint8_t* st = sm + s * kStageBytes;
             WAIT_OR_ABORT(&full[s], (uint32_t)((i / kStages) & 1));
-            const ChunkInfo ci = sInfo[s];
-            // outputs of chunk i-1 leave TMEM before MMA1(i) overwrites them
-            if (i > 0) stage_output();
-            // snapshot: bf16 S^T for MMA1, and S^T <- S^T Diag(gamma) for MMA2
+            // snapshot: bf16 S^T for MMA1, and S^T <- S^T Diag(gamma) for MMA2s
             {
                 const float4* gam4 =
                     reinterpret_cast<const float4*>(st + kRecGam) + 16 * hc;  // 64 channels
 #pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 16) {
-                    uint32_t r[16];
-                    float gam[16];
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    uint32_t r[2][16];
+                    tmem_ld16(lane_base + kColS + 64 * hc + c0, r[0]);
+                    tmem_ld16(lane_base + kColS + 64 * hc + c0 + 16, r[1]);
+                    float gam[32];
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) {
+                    for (int w = 0; w < 8; ++w) {
                         const float4 g4 = gam4[c0 / 4 + w];
                         gam[4 * w] = g4.x;
                         gam[4 * w + 1] = g4.y;
                         gam[4 * w + 2] = g4.z;
                         gam[4 * w + 3] = g4.w;
                     }
-                    tmem_load16(lane_base + kColS + 64 * hc + c0, r);
-                    uint32_t pk[8];
+                    tmem_wait_ld();
+                    reg_fence16(r[0]);
+                    reg_fence16(r[1]);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        pk[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
-                    tmem_st8(lane_base + kColSb + 32 * hc + c0 / 2, pk);
+                    for (int g = 0; g < 2; ++g) {
+                        uint32_t pk[8];
 #pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        r[u] = __float_as_uint(__uint_as_float(r[u]) * gam[u]);
-                    tmem_st16(lane_base + kColS + 64 * hc + c0, r);
+                        for (int u = 0; u < 8; ++u)
+                            pk[u] = pack_bf16(__uint_as_float(r[g][2 * u]),
+                                              __uint_as_float(r[g][2 * u + 1]));
+                        tmem_st8(lane_base + kColSb + 32 * hc + (c0 + 16 * g) / 2, pk);
+#pragma unroll
+                        for (int u = 0; u < 16; ++u)
+                            r[g][u] = __float_as_uint(__uint_as_float(r[g][u]) * gam[16 * g + u]);
+                        tmem_st16(lane_base + kColS + 64 * hc + c0 + 16 * g, r[g]);
+                    }
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&s_ready);
             }
-            if (i > 0) flush_output();  // overlaps MMA1(i)
             // Delta^T[v][t] = U[t][v] - X_W[v][t] for this thread's 32 tokens
             uint32_t uw[16];
             {
@@ -257,35 +237,29 @@ __global__ void __launch_bounds__(kThreads, 1) recur_t_kernel(const RecurTArgs P
             WAIT_OR_ABORT(&mma1, ph);
             tc_fence_after();
             {
+                uint32_t r[2][16];
+                tmem_ld16(lane_base + col_x(i) + 32 * hc, r[0]);
+                tmem_ld16(lane_base + col_x(i) + 32 * hc + 16, r[1]);
+                tmem_wait_ld();
+                reg_fence16(r[0]);
+                reg_fence16(r[1]);
                 uint32_t pk[16];
 #pragma unroll
-                for (int c0 = 0; c0 < 32; c0 += 16) {
-                    uint32_t r[16];
-                    tmem_load16(lane_base + kColX + 32 * hc + c0, r);
-#pragma unroll
-                    for (int u = 0; u < 16; u += 2) {
-                        const uint32_t uu = uw[(c0 + u) / 2];
-                        const float x0 = __uint_as_float(r[u]), x1 = __uint_as_float(r[u + 1]);
-                        xw[c0 + u] = x0;
-                        xw[c0 + u + 1] = x1;
-                        pk[(c0 + u) / 2] = pack_bf16(bf16_lo(uu) - x0, bf16_hi(uu) - x1);
-                    }
+                for (int u = 0; u < 32; u += 2) {
+                    const uint32_t uu = uw[u / 2];
+                    const float x0 = __uint_as_float(r[u >> 4][u & 15]);
+                    const float x1 = __uint_as_float(r[u >> 4][(u & 15) + 1]);
+                    pk[u / 2] = pack_bf16(bf16_lo(uu) - x0, bf16_hi(uu) - x1);
                 }
                 tmem_st16(lane_base + kColDb + 16 * hc, pk);
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&d_ready);
             }
-            WAIT_OR_ABORT(&mma2, ph);
+            WAIT_OR_ABORT(&mma2s, ph);
             tc_fence_after();
-            prev_tok0 = ci.tok0;
-            prev_len = ci.len;
         }
         if (!*((volatile int*)&s_abort)) {
-            if (nchunks > 0) {
-                stage_output();
-                flush_output();
-            }
             if constexpr (!std::is_same<HT, NoState>::value) {
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 16) {
@@ -302,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) recur_t_kernel(const RecurTArgs P
         tc_fence_before();
         __syncthreads();  // matches the epilogue warps' barrier after the initial state
         tc_fence_after();
-        if (warp == kEpiWarps) {
+        if (warp == kWarpProducer) {
             // ---------------------------------------------------- producer
             if (lane == 0) {
                 int fills[kStages] = {0, 0};
@@ -318,7 +292,6 @@ __global__ void __launch_bounds__(kThreads, 1) recur_t_kernel(const RecurTArgs P
                         bulk_prefetch_l2(
                             P.records + ((size_t)(c_begin + i + kAhead) * H + h) * kRecBytes,
                             kRecBytes);
-                    sInfo[s] = P.info[c_begin + i];  // published by the arrive below
                     mbar_arrive_expect_tx(&full[s], kRecBytes);
                     bulk_g2s(sm + s * kStageBytes,
                              P.records + ((size_t)(c_begin + i) * H + h) * kRecBytes, kRecBytes,
@@ -330,28 +303,34 @@ __global__ void __launch_bounds__(kThreads, 1) recur_t_kernel(const RecurTArgs P
                     if (fills[s] > 0 && !mbar_wait(&full[s], (uint32_t)((fills[s] - 1) & 1)))
                         atomicOr(P.status, kStatusTimeout);
             }
-        } else {
+        } else if (warp == kWarpMma) {
             // ---------------------------------------------------- MMA issuer
             const uint32_t idesc1 = idesc_bf16_f32(128, 128, false, true);
-            const uint32_t idesc2 = idesc_bf16_f32(128, 256, false, false);
+            const uint32_t idesc2 = idesc_bf16_f32(128, 128, false, false);
+            const uint32_t idesc3 = idesc_bf16_f32(128, 64, false, false);
             const uint32_t st0 = smem_addr(sm);
             // B operands of stage 0; stage s adds s * kStageBytes to the address
             // field (bytes >> 4), one K=16 step adds 256 B (16)
             const uint64_t dWQ0 = smem_desc(st0 + kRecWQ, 128, 2048);
-            const uint64_t dKA0 = smem_desc(st0 + kRecKT, 128, 1024);
+            const uint64_t dKT0 = smem_desc(st0 + kRecKT, 128, 1024);
+            const uint64_t dAQ0 = smem_desc(st0 + kRecAQ, 128, 1024);   // Aqk hi
+            const uint64_t dAQL0 = smem_desc(st0 + kRecAQL, 128, 1024); // Aqk lo
             constexpr uint64_t kStageStep = kStageBytes >> 4;
             for (int i = 0; i < nchunks; ++i) {
                 const int s = i % kStages;
                 const uint32_t ph = (uint32_t)(i & 1);
                 const uint64_t so = (uint64_t)s * kStageStep;
+                const uint32_t tX = tbase + col_x(i);
                 WAIT_OR_ABORT(&full[s], (uint32_t)((i / kStages) & 1));
+                // X[i % 2] still holds the outputs of chunk i - 2 until they are read
+                if (i >= 2) WAIT_OR_ABORT(&x_free[i & 1], (uint32_t)(((i - 2) >> 1) & 1));
                 WAIT_OR_ABORT(&s_ready, ph);
                 tc_fence_after();
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16_ta(tbase + kColX, tbase + kColSb + 8 * kk, dWQ0 + so + 16u * kk,
-                                    idesc1, kk > 0 ? 1u : 0u);
+                        mma_bf16_ta(tX, tbase + kColSb + 8 * kk, dWQ0 + so + 16u * kk, idesc1,
+                                    kk > 0 ? 1u : 0u);
                     mma_commit(&mma1);
                 }
                 __syncwarp();
@@ -360,12 +339,57 @@ __global__ void __launch_bounds__(kThreads, 1) recur_t_kernel(const RecurTArgs P
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ta(tbase + kColS, tbase + kColDb + 8 * kk, dKA0 + so + 16u * kk,
+                        mma_bf16_ta(tbase + kColS, tbase + kColDb + 8 * kk, dKT0 + so + 16u * kk,
                                     idesc2, 1u);
-                    mma_commit(&mma2);
+                    mma_commit(&mma2s);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ta(tX + 64, tbase + kColDb + 8 * kk, dAQ0 + so + 16u * kk, idesc3,
+                                    1u);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ta(tX + 64, tbase + kColDb + 8 * kk, dAQL0 + so + 16u * kk,
+                                    idesc3, 1u);
+                    mma_commit(&mma2o[i & 1]);
                     mma_commit(&empty[s]);
                 }
                 __syncwarp();
+            }
+        } else {
+            // ---------------------------------------------------- output warps
+            const int q = warp & 3;          // TMEM lane quarter
+            const int v = 32 * q + lane;     // value channel
+            const int ot = tid - 32 * kWarpOut0;  // 0..127
+            for (int i = 0; i < nchunks; ++i) {
+                const int b = i & 1;
+                WAIT_OR_ABORT(&mma2o[b], (uint32_t)((i >> 1) & 1));
+                tc_fence_after();
+                __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(sm + kSmemO + b * kTileO);
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    uint32_t r[2][16];
+                    tmem_ld16(taddr(tbase, 32u * q, col_x(i) + 64 + c0), r[0]);
+                    tmem_ld16(taddr(tbase, 32u * q, col_x(i) + 64 + c0 + 16), r[1]);
+                    tmem_wait_ld();
+                    reg_fence16(r[0]);
+                    reg_fence16(r[1]);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u)
+                        tile[(c0 + u) * kDim + v] = __float2bfloat16_rn(__uint_as_float(r[u >> 4][u & 15]));
+                }
+                tc_fence_before();
+                mbar_arrive(&x_free[b]);  // MMA1(i + 2) may overwrite X[b]
+                asm volatile("bar.sync 2, %0;" ::"r"(32 * kOutWarps) : "memory");
+                const ChunkInfo ci = P.info[c_begin + i];
+#pragma unroll
+                for (int it = 0; it < (int)(kTileO / 16) / (32 * kOutWarps); ++it) {
+                    const int e = ot + 32 * kOutWarps * it;  // 16-byte piece
+                    const int t = e >> 4, piece = e & 15;
+                    if (t < ci.len)
+                        reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(P.out) +
+                                                 ((size_t)(ci.tok0 + t) * H + h) * kDim)[piece] =
+                            reinterpret_cast<const uint4*>(tile + t * kDim)[piece];
+                }
             }
         }
     }
