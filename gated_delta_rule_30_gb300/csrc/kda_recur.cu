@@ -16,17 +16,18 @@
 // by the first product is taken, so each chunk costs two dependent MMA
 // rounds.
 //
-// Warp roles (192 threads): warps 0-3 own the 4 TMEM lane quarters (state
-// snapshot / decay, Delta for rows 0-63, output rows 64-127, state I/O); warp
-// 4 streams records with bulk copies into a 2- or 3-stage ring (and prefetches
-// upcoming records into L2); warp 5 issues the
-// MMAs.  Only X = [W;Q].S, Delta and the state update are on the sequential
-// chain; the output update for chunk i has its own barrier and is issued right
-// after the state update, so the tensor pipe (which runs a CTA's MMAs in issue
-// order) executes it while the next snapshot is taken and the record slot is
-// released a chunk earlier than if it followed the next first MMA.  Every
-// mbarrier wait is bounded; on timeout the CTA records kStatusTimeout, stops,
-// waits (bounded) for its own copies and frees TMEM.
+// Warp roles (256 threads): warps 0-3 own the 4 TMEM lane quarters (state
+// snapshot / decay, Delta for rows 0-63, state I/O); warp 4 streams records
+// with bulk copies into a 2- or 3-stage ring (and prefetches upcoming records
+// into L2); warp 5 issues the MMAs; warps 6-7 (lane quarters 2-3, the output
+// rows of X) write the outputs of chunk j from X[j % 2] while later chunks
+// run and then release that buffer to the MMA warp.  Only X = [W;Q].S, Delta
+// and the state update are on the sequential chain; the output update for
+// chunk i has its own barriers and is issued right after the state update, so
+// the tensor pipe (which runs a CTA's MMAs in issue order) executes it while
+// the next snapshot is taken.  Every mbarrier wait is bounded; on timeout the
+// CTA records kStatusTimeout, stops, waits (bounded) for its own copies and
+// frees TMEM.
 #include <cuda_runtime.h>
 
 #include <type_traits>
@@ -37,7 +38,7 @@
 namespace kda {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 256;
 
 template <int VS>
 struct RecurLayout {
@@ -137,10 +138,10 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
     constexpr int kSlices = kDim / VS;
     extern __shared__ __align__(1024) uint8_t sm[];
     // full/empty: record ring; s_ready: snapshot written; mma1: X = [W;Q].S done;
-    // d_ready: Delta written; mma2s: state update done; mma2o: output update done
+    // d_ready: Delta written; mma2s: state update done; mma2o[b]: output update
+    // of the chunk in X[b] done; x_free[b]: the output warps have read X[b]
     constexpr int NS = L::kStages;
-    __shared__ uint64_t full[NS], empty[NS], s_ready, mma1, d_ready, mma2s, mma2o;
-    __shared__ ChunkInfo sInfo[NS];
+    __shared__ uint64_t full[NS], empty[NS], s_ready, mma1, d_ready, mma2s, mma2o[2], x_free[2];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
@@ -171,7 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
         mbar_init(&mma1, 1);
         mbar_init(&d_ready, 64);
         mbar_init(&mma2s, 1);
-        mbar_init(&mma2o, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&mma2o[b], 1);
+            mbar_init(&x_free[b], 64);
+        }
         mbar_fence_init();
         s_abort = 0;
     }
@@ -221,7 +225,6 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
                         kRecBytes);
                 uint8_t* st = sm + s * L::kStageBytes;
                 const uint8_t* rec = P.records + ((size_t)(c_begin + i) * H + h) * kRecBytes;
-                sInfo[s] = P.info[c_begin + i];  // published by the arrive below
                 mbar_arrive_expect_tx(&full[s], L::kLoadBytes);
                 bulk_g2s(st, rec, kRecOperands, &full[s]);
                 bulk_g2s(st + L::kStageUT, rec + kRecUT + v0 * 128, VS * 128, &full[s]);
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tXj, dAQL0 + so + 16u * kk, dd + 16u * kk, idesc2, 1u);
-                mma_commit(&mma2o);
+                mma_commit(&mma2o[j & 1]);
                 mma_commit(&empty[j % NS]);
             }
             __syncwarp();
@@ -278,6 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
             const uint32_t ph = (uint32_t)(i & 1);
             const uint32_t tX = tbase + VS * (1 + (i & 1));
             WAIT_OR_ABORT(&full[s], (uint32_t)((i / NS) & 1));
+            // X[i % 2] still holds the outputs of chunk i - 2 until they are read
+            if (i >= 2) WAIT_OR_ABORT(&x_free[i & 1], (uint32_t)(((i - 2) >> 1) & 1));
             WAIT_OR_ABORT(&s_ready, ph);
             tc_fence_after();
             const uint64_t so = (uint64_t)s * kStageStep;
@@ -300,40 +305,15 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
             __syncwarp();
             issue_out(i);
         }
-    } else {
+    } else if (warp < 4) {
         // ------------------------------------------------------------ state / epilogue warps
         const int row = tid;  // TMEM lane: key channel for S, token row for X
-        int prev_tok0 = 0, prev_len = 0;
-        auto store_output = [&](int j) {
-            // rows 64..127 of X[j & 1] hold the outputs of chunk j
-            const int t = row - 64;
-            const uint32_t tXj = tbase + VS * (1 + (j & 1));
-#pragma unroll
-            for (int c0 = 0; c0 < VS; c0 += 16) {
-                uint32_t r[16];
-                tmem_load16(taddr(tXj, 32u * warp, (uint32_t)c0), r);
-                if (t < prev_len) {
-                    uint4* dst = reinterpret_cast<uint4*>(
-                        reinterpret_cast<__nv_bfloat16*>(P.out) +
-                        ((size_t)(prev_tok0 + t) * H + h) * kDim + v0 + c0);
-                    dst[0] = make_uint4(pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1])),
-                                        pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3])),
-                                        pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5])),
-                                        pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7])));
-                    dst[1] = make_uint4(pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9])),
-                                        pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11])),
-                                        pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13])),
-                                        pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15])));
-                }
-            }
-        };
         int i = 0;
         for (; i < nchunks; ++i) {
             const int s = i % NS;
             const uint32_t ph = (uint32_t)(i & 1);
             const uint8_t* st = sm + s * L::kStageBytes;
             WAIT_OR_ABORT(&full[s], (uint32_t)((i / NS) & 1));
-            const ChunkInfo ci = sInfo[s];
             // snapshot S (bf16, MN-major B operand K=128 x N=VS) and decay it in TMEM
             {
                 const float gam = reinterpret_cast<const float*>(st + L::kStageGam)[row];
@@ -360,13 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
                 tc_fence_before();
                 mbar_arrive(&s_ready);
             }
-            if (warp >= 2) {
-                if (i > 0) {
-                    WAIT_OR_ABORT(&mma2o, (uint32_t)((i - 1) & 1));
-                    tc_fence_after();
-                    store_output(i - 1);
-                }
-            } else {
+            if (warp < 2) {
                 // Delta = U - X[0:64] for token row `row`, into Db[i & 1]
                 const uint16_t* ut = reinterpret_cast<const uint16_t*>(st + L::kStageUT);
                 uint32_t u_pk[VS / 2];  // U[row][c], two bf16 per register, read before waiting
@@ -401,18 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
             }
             WAIT_OR_ABORT(&mma2s, ph);
             tc_fence_after();
-            prev_tok0 = ci.tok0;
-            prev_len = ci.len;
         }
         if (!*((volatile int*)&s_abort)) {
-            if (warp >= 2 && nchunks > 0) {
-                if (mbar_wait(&mma2o, (uint32_t)((nchunks - 1) & 1))) {
-                    tc_fence_after();
-                    store_output(nchunks - 1);
-                } else {
-                    atomicOr(P.status, kStatusTimeout);
-                }
-            }
             if constexpr (!std::is_same<HT, NoState>::value) {
                 const int ch = row;
 #pragma unroll
@@ -422,6 +386,41 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
                     StateIO<HT>::store16(P.hT, state_base + (size_t)ch * kDim + v0 + c0, r);
                 }
             }
+        }
+    } else {
+        // ------------------------------------------------------------ output warps
+        // warps 6 and 7 (TMEM lane quarters 2 and 3: rows 64..127 of X) write
+        // the outputs of chunk j from X[j % 2], then release that buffer
+        const int t = 32 * (warp & 3) - 64 + lane;  // token row of the chunk
+        for (int j = 0; j < nchunks; ++j) {
+            WAIT_OR_ABORT(&mma2o[j & 1], (uint32_t)((j >> 1) & 1));
+            tc_fence_after();
+            const ChunkInfo cj = P.info[c_begin + j];
+            const uint32_t tXj = tbase + VS * (1 + (j & 1));
+#pragma unroll
+            for (int c0 = 0; c0 < VS; c0 += 32) {
+                uint32_t r[2][16];
+                tmem_ld16(taddr(tXj, 32u * (warp & 3), (uint32_t)c0), r[0]);
+                tmem_ld16(taddr(tXj, 32u * (warp & 3), (uint32_t)c0 + 16u), r[1]);
+                tmem_wait_ld();
+                reg_fence16(r[0]);
+                reg_fence16(r[1]);
+                if (t < cj.len) {
+                    uint4* dst = reinterpret_cast<uint4*>(
+                        reinterpret_cast<__nv_bfloat16*>(P.out) +
+                        ((size_t)(cj.tok0 + t) * H + h) * kDim + v0 + c0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t* x = r[q >> 1] + 8 * (q & 1);
+                        dst[q] = make_uint4(pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                                            pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                                            pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                                            pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&x_free[j & 1]);  // MMA1(j + 2) may overwrite X[j % 2]
         }
     }
     tc_fence_before();
