@@ -210,11 +210,13 @@ def device_status(device=None):
         _check(lib().kda_device_status(_stream_ptr(dev)))
 
 
-RECURRENCE_KERNELS = {"auto": 0, "sliced": 1, "transposed": 2}
+RECURRENCE_KERNELS = {"auto": 0, "sliced": 1, "transposed": 2, "fused": 3}
 
 
 def set_recurrence_kernel(kind: str = "auto"):
-    """Choose the recurrence kernel for later calls: "auto", "sliced" or "transposed"."""
+    """Choose the recurrence kernel for later calls: "auto", "sliced", "transposed" or "fused"
+    (chunk kernel and transposed recurrence in one cooperative launch; falls back to the
+    two-kernel path when the problem has too many (sequence, head) pairs for it)."""
     if kind not in RECURRENCE_KERNELS:
         raise ValueError(f"kind must be one of {sorted(RECURRENCE_KERNELS)}")
     _check(lib().kda_set_recurrence_kernel(RECURRENCE_KERNELS[kind]))

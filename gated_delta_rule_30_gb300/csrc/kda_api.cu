@@ -63,11 +63,10 @@ constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t workspace_bytes(int64_t max_chunks, int64_t N, int64_t H) {
     return 256 + align256((size_t)(N + 1) * sizeof(int32_t)) +
            align256((size_t)max_chunks * sizeof(ChunkInfo)) +
-           (size_t)max_chunks * (size_t)H * kRecBytes;
+           (size_t)max_chunks * (size_t)H * kRecBytes + align256(ready_bytes(max_chunks, H));
 }
 
 Workspace carve_workspace(void* base, int64_t max_chunks, int64_t N, int64_t H) {
-    (void)H;
     uint8_t* p = static_cast<uint8_t*>(base);
     Workspace w;
     w.flags = reinterpret_cast<int32_t*>(p);
@@ -77,6 +76,8 @@ Workspace carve_workspace(void* base, int64_t max_chunks, int64_t N, int64_t H) 
     w.info = reinterpret_cast<ChunkInfo*>(p);
     p += align256((size_t)max_chunks * sizeof(ChunkInfo));
     w.records = p;
+    p += (size_t)max_chunks * (size_t)H * kRecBytes;
+    w.ready = reinterpret_cast<int32_t*>(p);
     return w;
 }
 
@@ -281,9 +282,26 @@ kda_status_t run(const Problem& p, void* workspace, size_t workspace_size, cudaS
     stage_mark(0, st);
     cudaError_t e = launch_schedule(p, ws, status, st);
     stage_mark(1, st);
-    if (e == cudaSuccess) e = launch_prep(p, ws, status, st);
-    stage_mark(2, st);
-    if (e == cudaSuccess) e = launch_recur(p, ws, status, st, g_recur_kind);
+    // kind 3 asks for the fused launch; automatic selection takes it for few,
+    // long sequences
+    bool fused = false;
+    if (e == cudaSuccess && (g_recur_kind == 3 || g_recur_kind == 0) &&
+        fused_eligible(p, g_recur_kind == 3)) {
+        e = launch_fused(p, ws, status, st);
+        if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorNotSupported) {
+            cudaGetLastError();  // not resident on this device right now: run the two kernels
+            e = cudaSuccess;
+        } else {
+            fused = true;
+        }
+    }
+    if (!fused) {
+        if (e == cudaSuccess) e = launch_prep(p, ws, status, st);
+        stage_mark(2, st);
+        if (e == cudaSuccess) e = launch_recur(p, ws, status, st, g_recur_kind == 3 ? 2 : g_recur_kind);
+    } else {
+        stage_mark(2, st);
+    }
     stage_mark(3, st);
     kda_status_t rc = KDA_OK;
     if (e != cudaSuccess) rc = cuda_error(e, "kernel launch");
@@ -385,7 +403,8 @@ extern "C" int kda_abi_version(void) { return KDA_ABI_VERSION; }
 
 extern "C" kda_status_t kda_set_recurrence_kernel(int32_t kind) {
     clear_error();
-    if (kind < 0 || kind > 2) return set_error(KDA_ERR_INVALID_ARGUMENT, "kind must be 0, 1 or 2");
+    if (kind < 0 || kind > 3)
+        return set_error(KDA_ERR_INVALID_ARGUMENT, "kind must be 0, 1, 2 or 3");
     g_recur_kind = kind;
     return KDA_OK;
 }

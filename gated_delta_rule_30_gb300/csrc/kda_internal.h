@@ -61,6 +61,7 @@ struct Workspace {
     int32_t* chunk_off;   // [N + 1] chunk prefix offsets per sequence
     ChunkInfo* info;      // [max_chunks]
     uint8_t* records;     // [max_chunks][H][kRecBytes]
+    int32_t* ready;       // [max_chunks][H] record-complete flags (fused launch only)
 };
 
 struct Problem {
@@ -101,6 +102,15 @@ constexpr int kStatusTimeout = 2;
 // Kernel launchers (kda_prep.cu, kda_recur.cu, kda_recur_t.cu, kda_api.cu).
 cudaError_t launch_schedule(const Problem& p, const Workspace& ws, int* status, cudaStream_t st);
 cudaError_t launch_prep(const Problem& p, const Workspace& ws, int* status, cudaStream_t st);
+// Fused launch (kda_fused.cu): chunk kernel and transposed recurrence in one
+// cooperative kernel.  fused_eligible says whether this device and problem
+// can take it (forced: the caller asked for it explicitly).
+bool fused_eligible(const Problem& p, bool forced);
+cudaError_t launch_fused(const Problem& p, const Workspace& ws, int* status, cudaStream_t st);
+inline size_t ready_bytes(int64_t max_chunks, int64_t H) {
+    return (size_t)max_chunks * (size_t)H * sizeof(int32_t);
+}
+
 // recurrence: kind 0 = chosen from the problem shape, 1 = value-sliced, 2 = transposed
 cudaError_t launch_recur(const Problem& p, const Workspace& ws, int* status, cudaStream_t st,
                          int kind);

@@ -1,640 +1,17 @@
-// kda_prep.cu -- chunk kernel of the KDA forward pass: everything that does
-// not depend on the running state, for one 64-token chunk of one head.
-//
-// For the chunk's tokens t = 0..63 (padding t >= len behaves as q = k = v = 0,
-// beta = 0, log-decay 0) and key channel c, with alpha_t = exp(la_t),
-//   la_t      = max(-exp(A_log[h]) * softplus(g_t + dt_bias[h]), lower_bound)
-//   E_t       = prod_{s<=t} alpha_s               = exp(G_t)
-//   F_t       = prod_{t<s<=63} alpha_s            = exp(G_last - G_t)
-//   A[i][j]   = beta_i sum_c k_ic k_jc exp(G_ic - G_jc)       (j < i)
-//   Aqk[i][j] = sum_c q_ic k_jc exp(G_ic - G_jc)              (j <= i)
-//   T         = (I + A)^-1 (unit lower triangular)
-//   W         = T diag(beta) (K o E),  U = T diag(beta) V
-// and writes W, scale*(Q o E), (K o F)^T, scale*Aqk (as a bf16 hi/lo pair),
-// U^T and exp(G_last) in the layout of one record (see kda_internal.h).  This
-// is the chunkwise form of the gated delta rule (reading of "Flashkda Delta
-// Attention", "Core Kernel API"; the pages give only the call), with the
-// exponentials of G differences factored per 16-token sub-block so that no
-// factor overflows fp32/bf16: for rows in sub-block a the reference point is
-// token m_a = 16a + 7,
-//   left_i  = x_i o exp(G_i - G_{m_a})     (x = k or q),
-//   right_j = k_j o exp(G_{m_a} - G_j)     (j < 16(a+1)),
-// so |exponent| <= 8 |lower_bound| inside a sub-block and <= 0 across them.
-// Every exp(G_i - G_j) is a product of the alphas between i and j, so the
-// only transcendentals are those of the gate itself.
-//
-// The kernel is persistent (two CTAs per SM, each looping over (chunk, head)
-// items): once an item's last MMA has read shared memory, the copies of the
-// next item's q, k, v, g are issued, so they land while the current item's
-// results are written out.
-//
-// Work split (256 threads): for the gate, the decays and the scaled operands
-// thread (c, h) owns key channel c = tid % 128 and the 32 tokens of half
-// h = tid / 128 of the chunk (products that cross the halves are exchanged
-// through shared memory).  The score products (M = 128 rows = the k and q
-// rows of the four sub-blocks, N = 16 + 32 + 48 + 64 = 160 columns holding
-// the four right operands side by side, K = 128 channels; the rows of
-// sub-block a only read the columns of its own right operand) and the two WY
-// products (M = 128 channels, N = 64 tokens,
-// K = 64 tokens) run on tcgen05 with fp32 accumulators in TMEM.  The
-// triangular inverse is blocked: the four 16 x 16 diagonal blocks by forward
-// substitution (one warp each), then the off-diagonal blocks level by level,
-// T_ab = -T_aa sum_{b<=c<a} A_ac T_cb, in fp32 shared memory.
-#include <cuda_runtime.h>
-
-#include "kda_internal.h"
-#include "tc.cuh"
+// kda_prep.cu -- stand-alone chunk kernel of the KDA forward pass (the worker
+// body and its design notes are in kda_prep.cuh).
+#include "kda_prep.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kThreads = 256;
-// shared memory map (bytes)
-constexpr uint32_t kSmQ = 0, kSmK = 16384, kSmV = 32768, kSmG = 49152;  // staging tiles [64][128]
-constexpr uint32_t kSmLeft = 0;       // 32 KB   (aliases staging once it is consumed)
-constexpr uint32_t kSmR = 32768;      // 40 KB   R_0..R_3
-constexpr uint32_t kSmVbT = 73728;    // 16 KB   (beta V)^T, K-major, M = 128 value channels, K = 64
-constexpr uint32_t kSmKbT = 90112;    // 16 KB   (beta K o E)^T
-constexpr uint32_t kSmBytes = 106496;
-// after the score MMAs (alias Left / R)
-constexpr int kStr = 68;              // fp32 row stride of the 64 x 64 tiles
-constexpr uint32_t kSmA = 0;          // A^T (beta-scaled, strictly lower A), fp32 [64][kStr]
-constexpr uint32_t kSmT = 17408;      // T, fp32 [64][kStr]
-constexpr uint32_t kSmX = 34816;      // level products, fp32 [3][16][16]
-constexpr uint32_t kSmTT = 40960;     // T^T as MN-major B operand, bf16 8 KB
-// R_a (16(a+1) rows x 256 B) starts at 2048 a (a+1): 0, 4096, 12288, 24576
-__host__ __device__ constexpr uint32_t r_off(int a) { return 2048u * a * (a + 1); }
-// score block a occupies TMEM columns [8 a (a+1), 8 (a+1)(a+2)): 0, 16, 48, 96
-__host__ __device__ constexpr uint32_t d_col(int a) { return 8u * a * (a + 1); }
-constexpr uint32_t kTmemCols = 256;
-
-struct PrepArgs {
-    const __nv_bfloat16* q;
-    const __nv_bfloat16* k;
-    const __nv_bfloat16* v;
-    const __nv_bfloat16* g;
-    const __nv_bfloat16* beta;
-    const float* A_log;
-    const float* dt_bias;
-    float lower_bound;
-    float scale;
-    int H;
-    int N;
-    const int32_t* flags;
-    const int32_t* chunk_off;
-    const ChunkInfo* info;
-    uint8_t* records;
-    int* status;
-};
-
-__device__ __forceinline__ float lds_bf16(const uint8_t* base, uint32_t off) {
-    return bf16_to_f(*reinterpret_cast<const uint16_t*>(base + off));
-}
-__device__ __forceinline__ void stg_v4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
-}
-__device__ __forceinline__ void sts_v4f(uint32_t saddr, const float (&x)[8]) {
-    st_shared_v4(saddr, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-                 pack_bf16(x[6], x[7]));
-}
-__device__ __forceinline__ void stg_v4f(uint8_t* p, const float (&x)[8]) {
-    stg_v4(p, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-           pack_bf16(x[6], x[7]));
-}
-
-// Right factors of one sub-block pair owned by a half: for the local block
-// b0 (tokens 0..15 of the half, reference 7) and b1 (tokens 16..31,
-// reference 23), rf0[u] = exp(G_{7} - G_u) for u < 16 and rf1[u] =
-// exp(G_{23} - G_u) for u < 32 (local token indices).
-__device__ __forceinline__ void right_factors(const float (&al)[32], float (&rf0)[16],
-                                              float (&rf1)[32]) {
-    float run = 1.f;
-    rf0[7] = 1.f;
-#pragma unroll
-    for (int u = 6; u >= 0; --u) {
-        run *= al[u + 1];
-        rf0[u] = run;
-    }
-    run = 1.f;
-#pragma unroll
-    for (int u = 15; u > 7; --u) {
-        rf0[u] = run;
-        run *= al[u];
-    }
-    float inv = 1.f / run;
-#pragma unroll
-    for (int u = 8; u < 16; ++u) rf0[u] *= inv;
-    run = 1.f;
-    rf1[23] = 1.f;
-#pragma unroll
-    for (int u = 22; u >= 0; --u) {
-        run *= al[u + 1];
-        rf1[u] = run;
-    }
-    run = 1.f;
-#pragma unroll
-    for (int u = 31; u > 23; --u) {
-        rf1[u] = run;
-        run *= al[u];
-    }
-    inv = 1.f / run;
-#pragma unroll
-    for (int u = 24; u < 32; ++u) rf1[u] *= inv;
-}
+using namespace prep;
 
 __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ float sBeta[kChunk];
-    __shared__ float sTot[2][kDim];   // product of each half's alphas
-    __shared__ float sQf[2][kDim];    // prod_{s=32}^{39} and prod_{s=32}^{55} alpha_s
-    __shared__ uint64_t bar;
-    __shared__ uint32_t tmem_base;
-    __shared__ int s_abort;
-
-    if (P.flags[0] != 1) return;
-    // a CTA that already gave up on a bounded wait poisons the launch: skip the rest
-    if (*((volatile int*)P.status) & kStatusTimeout) return;
-    const int H = P.H;
-    const int n_items = P.chunk_off[P.N] * H;  // valid (chunk, head) pairs
-    int item = blockIdx.x;
-    if (item >= n_items) return;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int ch = tid & (kDim - 1);
-    const int half = tid >> 7;
-    const int t0 = 32 * half;  // first token of this thread's half
-
-    // Issue the asynchronous copies of one item's q, k, v, g tiles (g in its
-    // own cp.async group, so the gate can start before q, k, v land) and set
-    // its beta.
-    auto stage = [&](const ChunkInfo& c, int hh, float beta_t) {
-        const __nv_bfloat16* srcs[4] = {P.g, P.q, P.k, P.v};
-        const uint32_t dsts[4] = {kSmG, kSmQ, kSmK, kSmV};
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int e = tid + kThreads * it;
-                const int row = e >> 4, col = e & 15;
-                const bool ok = row < c.len;
-                const __nv_bfloat16* src =
-                    srcs[x] + ((size_t)(ok ? c.tok0 + row : c.tok0) * H + hh) * kDim + col * 8;
-                cp_async16_zfill(sm + dsts[x] + row * 256 + col * 16, src, ok);
-            }
-            if (x == 0) cp_async_commit();
-        }
-        cp_async_commit();
-        if (tid < kChunk) sBeta[tid] = beta_t;
-    };
-    auto load_beta = [&](const ChunkInfo& c, int hh) -> float {
-        return (tid < c.len) ? __bfloat162float(P.beta[(size_t)(c.tok0 + tid) * H + hh]) : 0.f;
-    };
-
-    if (warp == 0) {
-        tmem_alloc(&tmem_base, kTmemCols);
-        tmem_relinquish();
-    }
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        mbar_fence_init();
-        s_abort = 0;
-    }
-    int chunk = item / H;
-    int h = item - chunk * H;
-    ChunkInfo ci = P.info[chunk];
-    stage(ci, h, tid < kChunk ? load_beta(ci, h) : 0.f);
-    float dtb = P.dt_bias[h * kDim + ch];
-    float alog = P.A_log[h];
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = tmem_base;
-
-    for (;;) {
-    const int len = ci.len;
-    uint8_t* rec = P.records + ((size_t)chunk * H + h) * kRecBytes;
-    // the next item's chunk info and per-head parameters, loaded early
-    const int next = item + (int)gridDim.x;
-    const bool has_next = next < n_items;
-    const int chunk_n = has_next ? next / H : chunk;
-    const int h_n = has_next ? next - chunk_n * H : h;
-    const ChunkInfo ci_n = P.info[chunk_n];
-    const float dtb_n = P.dt_bias[h_n * kDim + ch];
-    const float alog_n = P.A_log[h_n];
-    cp_async_wait_group<1>();  // this thread's g copies
-    __syncthreads();
-
-    // ---------------------------------------------------------------- gate (32 tokens)
-    float al[32];
-    {
-        // In base 2: x2 = (g + dt_bias) log2(e); softplus(x) log2(e) = max(x2, 0) +
-        // log2(1 + 2^-|x2|); log2(alpha) = max(-exp(A_log) * that, lower_bound log2(e)).
-        constexpr float kLog2e = 1.4426950408889634f;
-        const float dtb2 = dtb * kLog2e;
-        const float negA = -__expf(alog);
-        const float lb2 = P.lower_bound * kLog2e;
-        float prod = 1.f;
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const int t = t0 + u;
-            const float x2 = fmaf(lds_bf16(sm, kSmG + t * 256 + ch * 2), kLog2e, dtb2);
-            const float sp2 = fmaxf(x2, 0.f) + hw_log2(1.f + hw_exp2(-fabsf(x2)));
-            const float a = hw_exp2(fmaxf(negA * sp2, lb2));
-            al[u] = (t < len) ? a : 1.f;
-            prod *= al[u];
-            if (half == 1 && u == 7) sQf[0][ch] = prod;   // prod_{32}^{39}
-            if (half == 1 && u == 23) sQf[1][ch] = prod;  // prod_{32}^{55}
-        }
-        sTot[half][ch] = prod;
-    }
-    cp_async_wait_group<0>();  // q, k, v
-    __syncthreads();           // q, k, v, sTot, sQf visible
-    uint32_t qp[16], kp[16];
-#pragma unroll
-    for (int u = 0; u < 32; u += 2) {
-        const int t = t0 + u;
-        qp[u / 2] = pack_bf16(lds_bf16(sm, kSmQ + t * 256 + ch * 2),
-                              lds_bf16(sm, kSmQ + (t + 1) * 256 + ch * 2));
-        kp[u / 2] = pack_bf16(lds_bf16(sm, kSmK + t * 256 + ch * 2),
-                              lds_bf16(sm, kSmK + (t + 1) * 256 + ch * 2));
-    }
-#define KV(u) ((u) & 1 ? bf16_hi(kp[(u) / 2]) : bf16_lo(kp[(u) / 2]))
-#define QV(u) ((u) & 1 ? bf16_hi(qp[(u) / 2]) : bf16_lo(qp[(u) / 2]))
-    const float P0 = sTot[0][ch], P1 = sTot[1][ch];
-    {
-        // prefix pass: (beta K o E)^T to smem, scale * (Q o E) to the record
-        float E = half ? P0 : 1.f;
-#pragma unroll
-        for (int tg = 0; tg < 4; ++tg) {
-            float kb[8], qh[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int uu = tg * 8 + u;
-                E *= al[uu];
-                kb[u] = sBeta[t0 + uu] * KV(uu) * E;
-                qh[u] = P.scale * QV(uu) * E;
-            }
-            sts_v4f(smem_addr(sm + kSmKbT + kmaj_off(ch, t0 + tg * 8, 128, 1024)), kb);
-            stg_v4f(rec + kRecWQ + mnmaj_off(64 + t0 + tg * 8, ch, 128, 2048), qh);
-        }
-        if (half == 0) reinterpret_cast<float*>(rec + kRecGam)[ch] = P0 * P1;
-        // suffix pass: (K o F)^T to the record
-        float F = half ? 1.f : P1;
-#pragma unroll
-        for (int tg = 3; tg >= 0; --tg) {
-            float kt[8];
-#pragma unroll
-            for (int u = 7; u >= 0; --u) {
-                const int uu = tg * 8 + u;
-                kt[u] = KV(uu) * F;
-                F *= al[uu];
-            }
-            stg_v4f(rec + kRecKT + kmaj_off(ch, t0 + tg * 8, 128, 1024), kt);
-        }
-        // (beta V)^T (thread = value channel)
-#pragma unroll
-        for (int tg = 0; tg < 4; ++tg) {
-            float vb[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int t = t0 + tg * 8 + u;
-                vb[u] = sBeta[t] * lds_bf16(sm, kSmV + t * 256 + ch * 2);
-            }
-            sts_v4f(smem_addr(sm + kSmVbT + kmaj_off(ch, t0 + tg * 8, 128, 1024)), vb);
-        }
-    }
-    __syncthreads();  // staging fully consumed; Left / R may now overwrite it
-
-    // ---------------------------------------------------------------- score operands
-    {
-        // left factors exp(G_i - G_{m_a}) for this half's two sub-blocks
-#pragma unroll
-        for (int bl = 0; bl < 2; ++bl) {
-            const int a = 2 * half + bl;  // global sub-block
-            const int u0 = 16 * bl;       // its first local token
-            float lf[16];
-            float run = 1.f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                run *= al[u0 + u];
-                lf[u] = run;
-            }
-            const float inv = 1.f / lf[7];
-#pragma unroll
-            for (int u = 0; u < 7; ++u) lf[u] *= inv;
-            lf[7] = 1.f;
-            run = 1.f;
-#pragma unroll
-            for (int u = 8; u < 16; ++u) {
-                run *= al[u0 + u];
-                lf[u] = run;
-            }
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float kl[8], ql[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    kl[u] = KV(u0 + hh * 8 + u) * lf[hh * 8 + u];
-                    ql[u] = QV(u0 + hh * 8 + u) * lf[hh * 8 + u];
-                }
-                sts_v4f(smem_addr(sm + kSmLeft + mnmaj_off(16 * a + 8 * hh, ch, 128, 2048)), kl);
-                sts_v4f(smem_addr(sm + kSmLeft + mnmaj_off(64 + 16 * a + 8 * hh, ch, 128, 2048)),
-                        ql);
-            }
-        }
-        // right operands inside this half: R_{2h} rows [32h, 32h+16), R_{2h+1} rows [32h, 32h+32)
-        {
-            float rf0[16], rf1[32];
-            right_factors(al, rf0, rf1);
-            const int a0 = 2 * half, a1 = 2 * half + 1;
-#pragma unroll
-            for (int jg = 0; jg < 2; ++jg) {
-                float r8[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) r8[u] = KV(jg * 8 + u) * rf0[jg * 8 + u];
-                sts_v4f(smem_addr(sm + kSmR + r_off(a0) + mnmaj_off(t0 + jg * 8, ch, 128, 2048)),
-                        r8);
-            }
-#pragma unroll
-            for (int jg = 0; jg < 4; ++jg) {
-                float r8[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) r8[u] = KV(jg * 8 + u) * rf1[jg * 8 + u];
-                sts_v4f(smem_addr(sm + kSmR + r_off(a1) + mnmaj_off(t0 + jg * 8, ch, 128, 2048)),
-                        r8);
-            }
-        }
-        if (half == 0) {
-            // R_2 and R_3 rows [0, 32): prod_{j+1}^{31} alpha (local) times the
-            // second half's prod_{32}^{m_a} alpha
-            const float q2 = sQf[0][ch], q3 = sQf[1][ch];
-            float run = 1.f;
-            float sfx[32];
-#pragma unroll
-            for (int u = 31; u >= 0; --u) {
-                sfx[u] = run;
-                run *= al[u];
-            }
-#pragma unroll
-            for (int jg = 0; jg < 4; ++jg) {
-                float r2[8], r3[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float kv = KV(jg * 8 + u) * sfx[jg * 8 + u];
-                    r2[u] = kv * q2;
-                    r3[u] = kv * q3;
-                }
-                sts_v4f(smem_addr(sm + kSmR + r_off(2) + mnmaj_off(jg * 8, ch, 128, 2048)), r2);
-                sts_v4f(smem_addr(sm + kSmR + r_off(3) + mnmaj_off(jg * 8, ch, 128, 2048)), r3);
-            }
-        }
-    }
-#undef KV
-#undef QV
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---------------------------------------------------------------- score MMAs
-    if (tid == 0) {
-        // R_0..R_3 are contiguous with one 2048-B stride between 8-row groups and
-        // their TMEM columns d_col(a) follow the same order, so all four score
-        // blocks are one MMA with N = 16 + 32 + 48 + 64 = 160 (8 instructions).
-        tc_fence_after();
-        const uint64_t dl = smem_desc(smem_addr(sm + kSmLeft), 128, 2048);
-        const uint64_t dr = smem_desc(smem_addr(sm + kSmR), 128, 2048);
-        const uint32_t idesc = idesc_bf16_f32(128, 160, true, true);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_bf16(tbase, dl + 16u * kk, dr + 16u * kk, idesc, kk > 0 ? 1u : 0u);
-        mma_commit(&bar);
-    }
-    if (!mbar_wait(&bar, 0)) {
-        atomicOr(P.status, kStatusTimeout);
-        s_abort = 1;
-    }
-    tc_fence_after();
-    __syncthreads();
-    if (s_abort) break;
-
-    // ---------------------------------------------------------------- score read-out
-    // TMEM lane quarter w % 4 holds k rows (quarters 0, 1) or q rows (2, 3) of
-    // tokens 32 (w % 2) .. + 31, i.e. sub-blocks a_lo = 2 (w % 2) (lanes 0-15)
-    // and a_lo + 1 (lanes 16-31); warps w and w + 4 split that row's columns j.
-    {
-        const int qd = warp & 3, hj = warp >> 2;
-        const bool is_k = qd < 2;
-        const int i = 32 * (qd & 1) + lane;  // token of this row
-        const int a_lo = 2 * (qd & 1);
-        const bool upper = lane >= 16;       // row of sub-block a_lo + 1
-        const int jw = (qd & 1) ? 32 : 16;   // columns per warp
-        float* sAT = reinterpret_cast<float*>(sm + kSmA);
-        const float f = is_k ? sBeta[i] : P.scale;
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            if (rr * 16 >= jw) break;
-            const int jb = jw * hj + 16 * rr;
-            uint32_t r0[16], r1[16];
-            tmem_ld16(taddr(tbase, 32u * qd, d_col(a_lo) + (uint32_t)jb), r0);
-            tmem_ld16(taddr(tbase, 32u * qd, d_col(a_lo + 1) + (uint32_t)jb), r1);
-            tmem_wait_ld();
-            reg_fence16(r0);
-            reg_fence16(r1);
-            float val[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int j = jb + u;
-                const float x = __uint_as_float(upper ? r1[u] : r0[u]);
-                val[u] = (is_k ? (j < i) : (j <= i)) ? f * x : 0.f;
-            }
-            if (is_k) {
-                // A^T[j][i] = beta_i A[i][j] (column-major A: the inverse reads columns)
-#pragma unroll
-                for (int u = 0; u < 16; ++u) sAT[(jb + u) * kStr + i] = val[u];
-            } else {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float hi[8], lo[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        hi[u] = __bfloat162float(__float2bfloat16_rn(val[8 * hh + u]));
-                        lo[u] = val[8 * hh + u] - hi[u];
-                    }
-                    stg_v4f(rec + kRecAQ + kmaj_off(i, jb + 8 * hh, 128, 1024), hi);
-                    stg_v4f(rec + kRecAQL + kmaj_off(i, jb + 8 * hh, 128, 1024), lo);
-                }
-            }
-        }
-        if (qd == 2) {
-            // tokens 0..31 attend to no key in 32..63: zero those record columns
-#pragma unroll
-            for (int jg = 0; jg < 2; ++jg) {
-                const int j0 = 32 + 16 * hj + 8 * jg;
-                stg_v4(rec + kRecAQ + kmaj_off(i, j0, 128, 1024), 0u, 0u, 0u, 0u);
-                stg_v4(rec + kRecAQL + kmaj_off(i, j0, 128, 1024), 0u, 0u, 0u, 0u);
-            }
-        }
-        // zero the strictly upper 16 x 16 blocks of T
-        float* sT = reinterpret_cast<float*>(sm + kSmT);
-        for (int e = tid; e < 6 * 256; e += kThreads) {
-            const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-            const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            sT[(16 * a + r) * kStr + 16 * b + c] = 0.f;
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-
-    // ---------------------------------------------------------------- T = (I + A)^-1
-    {
-        const float* sAT = reinterpret_cast<const float*>(sm + kSmA);  // sAT[l][i] = A[i][l]
-        float* sT = reinterpret_cast<float*>(sm + kSmT);
-        float* sX = reinterpret_cast<float*>(sm + kSmX);
-        if (warp < 4 && lane < 16) {
-            // diagonal block `warp`, column `lane`, by forward substitution
-            const int o = 16 * warp, j = lane;
-            float tc[16];
-#pragma unroll
-            for (int l = 0; l < 16; ++l) tc[l] = (l == j) ? 1.f : 0.f;
-#pragma unroll
-            for (int i = 1; i < 16; ++i) {
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                for (int l = 0; l < i; ++l) {
-                    if (l & 1)
-                        s1 = fmaf(sAT[(o + l) * kStr + o + i], tc[l], s1);
-                    else
-                        s0 = fmaf(sAT[(o + l) * kStr + o + i], tc[l], s0);
-                }
-                if (i > j) tc[i] = -(s0 + s1);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) sT[(o + i) * kStr + o + j] = tc[i];
-        }
-        __syncthreads();
-        // off-diagonal blocks, one diagonal distance d at a time:
-        //   X_ab = sum_{c=b}^{a-1} A_ac T_cb ;  T_ab = -T_aa X_ab   (a = b + d)
-        // each thread computes a 2 x 2 tile (rows r, r+1; columns c, c+1)
-#pragma unroll
-        for (int d = 1; d < 4; ++d) {
-            const int nitems = (4 - d) * 64;
-            if (tid < nitems) {
-                const int b = tid >> 6, r = ((tid >> 3) & 7) * 2, c = (tid & 7) * 2;
-                const int a = b + d;
-                float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
-                for (int l = 16 * b; l < 16 * a; ++l) {
-                    const float2 av = *reinterpret_cast<const float2*>(sAT + l * kStr + 16 * a + r);
-                    const float2 tv = *reinterpret_cast<const float2*>(sT + l * kStr + 16 * b + c);
-                    x00 = fmaf(av.x, tv.x, x00);
-                    x01 = fmaf(av.x, tv.y, x01);
-                    x10 = fmaf(av.y, tv.x, x10);
-                    x11 = fmaf(av.y, tv.y, x11);
-                }
-                *reinterpret_cast<float2*>(sX + b * 256 + r * 16 + c) = make_float2(x00, x01);
-                *reinterpret_cast<float2*>(sX + b * 256 + (r + 1) * 16 + c) = make_float2(x10, x11);
-            }
-            __syncthreads();
-            if (tid < nitems) {
-                const int b = tid >> 6, r = ((tid >> 3) & 7) * 2, c = (tid & 7) * 2;
-                const int a = b + d;
-                float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
-#pragma unroll
-                for (int l = 0; l < 16; ++l) {
-                    const float t0v = sT[(16 * a + r) * kStr + 16 * a + l];
-                    const float t1v = sT[(16 * a + r + 1) * kStr + 16 * a + l];
-                    const float2 xv = *reinterpret_cast<const float2*>(sX + b * 256 + l * 16 + c);
-                    y00 = fmaf(t0v, xv.x, y00);
-                    y01 = fmaf(t0v, xv.y, y01);
-                    y10 = fmaf(t1v, xv.x, y10);
-                    y11 = fmaf(t1v, xv.y, y11);
-                }
-                *reinterpret_cast<float2*>(sT + (16 * a + r) * kStr + 16 * b + c) =
-                    make_float2(-y00, -y01);
-                *reinterpret_cast<float2*>(sT + (16 * a + r + 1) * kStr + 16 * b + c) =
-                    make_float2(-y10, -y11);
-            }
-            __syncthreads();
-        }
-        // T^T as MN-major B operand: element (n = t, k = s), k-groups 128 B, n-groups 1024 B
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int e = tid + kThreads * it;   // 512 vectors: (t-group, s)
-            const int s = e & 63, tg = e >> 6;
-            float x[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) x[u] = sT[(tg * 8 + u) * kStr + s];
-            sts_v4f(smem_addr(sm + kSmTT + mnmaj_off(tg * 8, s, 128, 1024)), x);
-        }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---------------------------------------------------------------- W^T, U^T MMAs
-    if (tid == 0) {
-        tc_fence_after();
-        const uint32_t idesc = idesc_bf16_f32(128, 64, false, true);
-        const uint32_t bT = smem_addr(sm + kSmTT);
-        const uint32_t aK = smem_addr(sm + kSmKbT);
-        const uint32_t aV = smem_addr(sm + kSmVbT);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tbase + 0, smem_desc(aK + kk * 256, 128, 1024),
-                     smem_desc(bT + kk * 256, 128, 1024), idesc, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tbase + 64, smem_desc(aV + kk * 256, 128, 1024),
-                     smem_desc(bT + kk * 256, 128, 1024), idesc, kk > 0 ? 1u : 0u);
-        mma_commit(&bar);
-    }
-    if (!mbar_wait(&bar, 1)) {
-        atomicOr(P.status, kStatusTimeout);
-        s_abort = 1;
-    }
-    tc_fence_after();
-    __syncthreads();
-    if (s_abort) break;
-
-    // the staging area is free again: start the next item's copies
-    float beta_n = 0.f;
-    if (has_next && tid < kChunk) beta_n = load_beta(ci_n, h_n);
-    if (has_next) stage(ci_n, h_n, beta_n);
-
-    // ---------------------------------------------------------------- W (warps 0-3), U^T (4-7)
-    {
-        const bool is_w = warp < 4;
-        const uint32_t col0 = is_w ? 0u : 64u;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t r[16];
-            tmem_load16(taddr(tbase, 32u * (warp & 3), col0 + 16u * c), r);
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float x[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) x[u] = __uint_as_float(r[8 * hh + u]);
-                if (is_w)
-                    stg_v4f(rec + kRecWQ + mnmaj_off(16 * c + 8 * hh, ch, 128, 2048), x);
-                else
-                    stg_v4f(rec + kRecUT + ch * 128 + (16 * c + 8 * hh) * 2, x);
-            }
-        }
-    }
-
-    if (!has_next) break;
-    item = next;
-    chunk = chunk_n;
-    h = h_n;
-    ci = ci_n;
-    dtb = dtb_n;
-    alog = alog_n;
-    tc_fence_before();
-    }  // item loop
-
-    cp_async_wait_all();
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, kTmemCols);
+    __shared__ PrepShared S;
+    // barrier 0 over the whole 256-thread CTA is __syncthreads
+    prep_body(P, sm, S, threadIdx.x, 0u, blockIdx.x, gridDim.x, nullptr, true);
 }
 
 }  // namespace
@@ -644,23 +21,7 @@ cudaError_t launch_prep(const Problem& p, const Workspace& ws, int* status, cuda
     cudaError_t e =
         cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmBytes);
     if (e != cudaSuccess) return e;
-    PrepArgs a;
-    a.q = reinterpret_cast<const __nv_bfloat16*>(p.q);
-    a.k = reinterpret_cast<const __nv_bfloat16*>(p.k);
-    a.v = reinterpret_cast<const __nv_bfloat16*>(p.v);
-    a.g = reinterpret_cast<const __nv_bfloat16*>(p.g);
-    a.beta = reinterpret_cast<const __nv_bfloat16*>(p.beta);
-    a.A_log = p.A_log;
-    a.dt_bias = p.dt_bias;
-    a.lower_bound = p.lower_bound;
-    a.scale = p.scale;
-    a.H = p.H;
-    a.N = p.N;
-    a.flags = ws.flags;
-    a.chunk_off = ws.chunk_off;
-    a.info = ws.info;
-    a.records = ws.records;
-    a.status = status;
+    const PrepArgs a = make_prep_args(p, ws, status);
     // persistent: two CTAs per SM, each looping over (chunk, head) items
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);

@@ -146,8 +146,11 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
     __shared__ int s_abort;
 
     if (P.flags[0] != 1) return;
-    // a CTA that already gave up on a bounded wait poisons the launch: skip the rest
-    if (*((volatile int*)P.status) & kStatusTimeout) return;
+    // a CTA that already gave up on a bounded wait poisons the launch: skip the
+    // rest (decided once, so every thread takes the same path)
+    if (threadIdx.x == 0) s_abort = (*((volatile int*)P.status) & kStatusTimeout) ? 1 : 0;
+    __syncthreads();
+    if (s_abort) return;
     const int H = P.H;
     const int slice = blockIdx.x % kSlices;
     const int nh = blockIdx.x / kSlices;

@@ -174,14 +174,17 @@ int kda_abi_version(void);
 kda_status_t kda_set_stage_events(void* const* events, int32_t count);
 
 /*
- * kda_set_recurrence_kernel -- selects the kernel that runs the sequential
- * chunk-to-chunk recurrence (no counterpart on the pages; every choice computes
- * the same operation to the same tolerance).  kind = 0 (default): chosen per
- * call from the number of (sequence, head) pairs and the SM count; 1: the
- * value-sliced kernel (state slices of 32..128 value channels, one CTA each);
- * 2: the transposed kernel (one CTA per (sequence, head), state held as S^T).
- * Process-wide, applies to later calls; not thread-safe.  Any other kind
- * returns KDA_ERR_INVALID_ARGUMENT.
+ * kda_set_recurrence_kernel -- selects how the sequential chunk-to-chunk
+ * recurrence runs (no counterpart on the pages; every choice computes the same
+ * operation to the same tolerance).  kind = 0 (default): chosen per call from
+ * the number of (sequence, head) pairs, the chunks per sequence and the SM
+ * count; 1: the value-sliced kernel (state slices of 32..128 value channels,
+ * one CTA each); 2: the transposed kernel (one CTA per (sequence, head), state
+ * held as S^T); 3: the fused launch (chunk kernel and transposed recurrence in
+ * one cooperative kernel, overlapping; used only when the pairs leave at
+ * least one SM for the chunk kernel, else kind 2 runs).  Process-wide,
+ * applies to later calls; not thread-safe.  Any other kind returns
+ * KDA_ERR_INVALID_ARGUMENT.
  */
 kda_status_t kda_set_recurrence_kernel(int32_t kind);
 

@@ -1,6 +1,7 @@
 """Parity of the CUDA path with the fp64 oracle (GPU).
 
-Every case runs once per recurrence kernel (value-sliced and transposed),
+Every case runs once per recurrence path (value-sliced, transposed, and the
+fused launch of chunk kernel and recurrence),
 draws seeded inputs with ``gated_delta_rule_30_gb300.inputs``,
 runs ``kda.fwd`` (through the C ABI) and compares the bf16 outputs and the
 final states with the oracle over the whole tensors: relative Frobenius error
@@ -19,7 +20,7 @@ from kda_testutil import (REC_BYTES, assert_close, decode_record, errors, read_s
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True, params=["sliced", "transposed"])
+@pytest.fixture(autouse=True, params=["sliced", "transposed", "fused"])
 def recur_kernel(request, kda_lib):
     kda_lib.set_recurrence_kernel(request.param)
     yield request.param
@@ -209,6 +210,23 @@ def test_auto_choice_is_one_of_the_kernels(kda_lib, recur_kernel):
         chosen = "transposed" if 2 * pairs >= sms else "sliced"
         if chosen == recur_kernel:
             assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_fused_matches_two_kernel_path(kda_lib, recur_kernel):
+    """The fused launch runs the same arithmetic as the chunk kernel followed by
+    the transposed recurrence: results are bit-identical, and automatic
+    selection takes it for few, long sequences."""
+    if recur_kernel != "fused":
+        pytest.skip("compares the fused launch with the transposed path")
+    for p in (make("long_context", T=4096, H=4), custom(lens=[700, 1, 2000], H=2, seed=9)):
+        o1, h1 = run_gpu(p)
+        kda_lib.set_recurrence_kernel("transposed")
+        o2, h2 = run_gpu(p)
+        kda_lib.set_recurrence_kernel("auto")
+        o3, h3 = run_gpu(p)
+        kda_lib.set_recurrence_kernel("fused")
+        assert torch.equal(o1, o2) and torch.equal(h1, h2)
+        assert torch.equal(o1, o3) and torch.equal(h1, h3)
 
 
 def test_malformed_cu_seqlens_reported(kda_lib):
