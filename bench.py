@@ -78,10 +78,19 @@ def workload_config(w, p, alg_bytes, head_tokens, flops, world):
             "counted_bytes_per_step": alg_bytes}
 
 
-def kernel_source_hash(src):
-    """Hash of a kernel's source and the headers it includes (ties ncu counters to a build)."""
+# sources that make up each timed kernel (the hash ties ncu counters to a build)
+KERNEL_SOURCES = {
+    "chunk": ("kda_prep.cu", "kda_prep.cuh"),
+    "recurrence/sliced": ("kda_recur.cu",),
+    "recurrence/transposed": ("kda_recur_t.cu", "kda_recur_t.cuh"),
+    "fused": ("kda_fused.cu", "kda_prep.cuh", "kda_recur_t.cuh"),
+}
+
+
+def kernel_source_hash(kernel):
+    """Hash of a kernel's sources and the headers they include."""
     h = hashlib.sha256()
-    for name in (src, "tc.cuh", "kda_internal.h"):
+    for name in KERNEL_SOURCES[kernel] + ("tc.cuh", "kda_internal.h"):
         with open(os.path.join(ROOT, "gated_delta_rule_30_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -269,6 +278,7 @@ def main():
         step()
     torch.cuda.synchronize(dev)
     kda.device_status(dev)
+    path = kda.last_path()  # "sliced" / "transposed": chunk kernel + recurrence; "fused": one launch
 
     # stage events: per-kernel durations measured on the launch stream
     n_ev = args.steps
@@ -304,11 +314,13 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_total = float(t.item())
     ms_step = ms_total / args.steps
-    stage_ms = {"schedule": [], "chunk": [], "recurrence": []}
+    # events: [0] before the schedule kernel, [1] after it, [2] after the chunk
+    # kernel (fused path: after the fused kernel), [3] after the recurrence
+    names = ("schedule", "fused") if path == "fused" else ("schedule", "chunk", "recurrence")
+    stage_ms = {k: [] for k in names}
     for row in evs:
-        stage_ms["schedule"].append(row[0].elapsed_time(row[1]))
-        stage_ms["chunk"].append(row[1].elapsed_time(row[2]))
-        stage_ms["recurrence"].append(row[2].elapsed_time(row[3]))
+        for j, k in enumerate(names):
+            stage_ms[k].append(row[j].elapsed_time(row[j + 1]))
     stage_avg = {k: sum(v) / len(v) for k, v in stage_ms.items()}
 
     # end to end: pinned host inputs -> device -> fwd -> outputs back to pinned host
@@ -344,16 +356,17 @@ def main():
         e2e_ms = float(t.item())
 
     hbm_peak, bf16_peak, peak_kind = peaks()
-    dominant = max(("chunk", "recurrence"), key=lambda k: stage_avg[k])
+    dominant = max((k for k in names if k != "schedule"), key=lambda k: stage_avg[k])
     dom_ms = stage_avg[dominant]
+    dom_kernel = dominant if dominant != "recurrence" else "recurrence/" + path
     achieved = alg_bytes / (dom_ms * 1e-3) / 1e9
     roofline_s = max(flops / (bf16_peak * 1e12), alg_bytes / (hbm_peak * 1e9))
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
-        h = kernel_source_hash({"chunk": "kda_prep.cu", "recurrence": "kda_recur.cu"}[dominant])
+        h = kernel_source_hash(dom_kernel)
         with open(tpath) as f:
-            tr = json.load(f).get(dominant, {})
+            tr = json.load(f).get(dom_kernel, {})
         if tr.get("source_sha256_16") == h and tr.get("workload") == args.workload:
             traffic = tr.get("bytes_per_launch")
 
@@ -366,13 +379,14 @@ def main():
         "tflops": flops / (ms_step * 1e-3) / 1e12,
         "roofline_fraction_step": roofline_s / (ms_step * 1e-3),
         "stage_ms": stage_avg,
-        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm_peak,
+        "path": path,
+        "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": achieved, "peak": hbm_peak,
                      "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
                      "peak_kind": peak_kind,
                      "note": "achieved = counted bytes of the whole pass / dominant kernel time"},
         "e2e": {"value": head_tokens * world / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": len(names) * args.steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

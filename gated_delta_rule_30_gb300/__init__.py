@@ -19,7 +19,7 @@ import ctypes
 import os
 
 __all__ = ["fwd", "lib", "library_path", "workspace_size", "device_status", "KDAError",
-           "selftest_tcgen05", "set_recurrence_kernel", "set_stage_events"]
+           "selftest_tcgen05", "set_recurrence_kernel", "set_stage_events", "last_path"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libkda.so")
@@ -68,6 +68,8 @@ def lib():
         L.kda_last_error_message.argtypes = []
         L.kda_abi_version.restype = ctypes.c_int
         L.kda_abi_version.argtypes = []
+        L.kda_last_path.restype = ctypes.c_int
+        L.kda_last_path.argtypes = []
         L.kda_set_recurrence_kernel.restype = ctypes.c_int
         L.kda_set_recurrence_kernel.argtypes = [i32]
         L.kda_set_stage_events.restype = ctypes.c_int
@@ -220,6 +222,14 @@ def set_recurrence_kernel(kind: str = "auto"):
     if kind not in RECURRENCE_KERNELS:
         raise ValueError(f"kind must be one of {sorted(RECURRENCE_KERNELS)}")
     _check(lib().kda_set_recurrence_kernel(RECURRENCE_KERNELS[kind]))
+
+
+PATHS = {1: "sliced", 2: "transposed", 3: "fused"}
+
+
+def last_path():
+    """How this thread's last forward pass ran: "sliced", "transposed", "fused" (None before any)."""
+    return PATHS.get(lib().kda_last_path())
 
 
 def set_stage_events(events):

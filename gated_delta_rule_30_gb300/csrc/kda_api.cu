@@ -17,6 +17,7 @@ namespace kda {
 // ----------------------------------------------------------------------------- errors
 namespace {
 thread_local char g_msg[512] = {0};
+thread_local int g_last_path = 0;  // kda_last_path
 }  // namespace
 
 kda_status_t set_error(kda_status_t s, const char* msg) {
@@ -296,11 +297,14 @@ kda_status_t run(const Problem& p, void* workspace, size_t workspace_size, cudaS
         }
     }
     if (!fused) {
+        const int kind = recur_choose(p, g_recur_kind == 3 ? 2 : g_recur_kind);
         if (e == cudaSuccess) e = launch_prep(p, ws, status, st);
         stage_mark(2, st);
-        if (e == cudaSuccess) e = launch_recur(p, ws, status, st, g_recur_kind == 3 ? 2 : g_recur_kind);
+        if (e == cudaSuccess) e = launch_recur(p, ws, status, st, kind);
+        g_last_path = kind;
     } else {
         stage_mark(2, st);
+        g_last_path = 3;
     }
     stage_mark(3, st);
     kda_status_t rc = KDA_OK;
@@ -398,6 +402,8 @@ extern "C" const char* kda_status_string(kda_status_t s) {
 }
 
 extern "C" const char* kda_last_error_message(void) { return kda::g_msg; }
+
+extern "C" int kda_last_path(void) { return kda::g_last_path; }
 
 extern "C" int kda_abi_version(void) { return KDA_ABI_VERSION; }
 

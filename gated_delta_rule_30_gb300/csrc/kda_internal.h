@@ -111,7 +111,9 @@ inline size_t ready_bytes(int64_t max_chunks, int64_t H) {
     return (size_t)max_chunks * (size_t)H * sizeof(int32_t);
 }
 
-// recurrence: kind 0 = chosen from the problem shape, 1 = value-sliced, 2 = transposed
+// recurrence: kind 0 = chosen from the problem shape, 1 = value-sliced, 2 = transposed;
+// recur_choose resolves kind 0 to 1 or 2
+int recur_choose(const Problem& p, int kind);
 cudaError_t launch_recur(const Problem& p, const Workspace& ws, int* status, cudaStream_t st,
                          int kind);
 cudaError_t launch_recur_sliced(const Problem& p, const Workspace& ws, int* status,

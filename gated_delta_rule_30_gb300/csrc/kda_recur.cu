@@ -504,16 +504,18 @@ bool recur_prefers_transposed(const Problem& p, int num_sms) {
     return 2LL * p.N * p.H >= num_sms;
 }
 
+int recur_choose(const Problem& p, int kind) {
+    if (kind == 1 || kind == 2) return kind;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return recur_prefers_transposed(p, sms) ? 2 : 1;
+}
+
 cudaError_t launch_recur(const Problem& p, const Workspace& ws, int* status, cudaStream_t st,
                          int kind) {
-    if (kind == 0) {
-        int dev = 0, sms = 148;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        kind = recur_prefers_transposed(p, sms) ? 2 : 1;
-    }
-    return kind == 2 ? launch_recur_transposed(p, ws, status, st)
-                     : launch_recur_sliced(p, ws, status, st);
+    return recur_choose(p, kind) == 2 ? launch_recur_transposed(p, ws, status, st)
+                                      : launch_recur_sliced(p, ws, status, st);
 }
 
 }  // namespace kda

@@ -159,6 +159,15 @@ const char* kda_status_string(kda_status_t status);
 /* Detail of the last error returned on the calling host thread (thread-local). */
 const char* kda_last_error_message(void);
 
+/*
+ * kda_last_path -- how the calling host thread's last successful kda_fwd /
+ * kda_fwd_ws / kda_fwd_noalloc call with a non-empty problem ran (no
+ * counterpart on the pages; for benchmarks and diagnostics): 1 = chunk kernel
+ * then value-sliced recurrence, 2 = chunk kernel then transposed recurrence,
+ * 3 = the fused cooperative launch; 0 before any such call.
+ */
+int kda_last_path(void);
+
 /* KDA_ABI_VERSION of the built library. */
 int kda_abi_version(void);
 

@@ -96,6 +96,19 @@ def test_stage_events_validation(kda_lib):
     assert L.kda_set_stage_events(arr, 3) == 1
 
 
+def test_recurrence_selection_validation(kda_lib):
+    L = ctypes.CDLL(kda_lib.library_path())
+    L.kda_set_recurrence_kernel.argtypes = [ctypes.c_int32]
+    for kind in (-1, 4, 99):
+        assert L.kda_set_recurrence_kernel(kind) == 1  # KDA_ERR_INVALID_ARGUMENT
+    for kind in (3, 2, 1, 0):
+        assert L.kda_set_recurrence_kernel(kind) == 0
+    with pytest.raises(ValueError):
+        kda_lib.set_recurrence_kernel("bogus")
+    # no forward pass has run on this thread
+    assert L.kda_last_path() == 0 and kda_lib.last_path() is None
+
+
 def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     import gated_delta_rule_30_gb300 as kda
     monkeypatch.setattr(kda, "_lib", None)
