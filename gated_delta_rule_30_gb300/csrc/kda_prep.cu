@@ -7,7 +7,7 @@ namespace {
 
 using namespace prep;
 
-__global__ void __launch_bounds__(kThreads, 2) prep_kernel(const PrepArgs P) {
+__global__ void __launch_bounds__(kThreads, 2) prep_kernel(const __grid_constant__ PrepArgs P) {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ PrepShared S;
     // barrier 0 over the whole 256-thread CTA is __syncthreads
@@ -21,7 +21,8 @@ cudaError_t launch_prep(const Problem& p, const Workspace& ws, int* status, cuda
     cudaError_t e =
         cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmBytes);
     if (e != cudaSuccess) return e;
-    const PrepArgs a = make_prep_args(p, ws, status);
+    PrepArgs a;
+    if (!make_prep_args(p, ws, status, a)) return cudaErrorInvalidValue;
     // persistent: two CTAs per SM, each looping over (chunk, head) items
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);

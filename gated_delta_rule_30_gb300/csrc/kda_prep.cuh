@@ -44,6 +44,7 @@
 // substitution (one warp each), then the off-diagonal blocks level by level,
 // T_ab = -T_aa sum_{b<=c<a} A_ac T_cb, in fp32 shared memory.
 #pragma once
+#include <cuda.h>  // CUtensorMap (the encoder is fetched at run time)
 #include <cuda_runtime.h>
 
 #include "kda_internal.h"
@@ -74,6 +75,9 @@ __host__ __device__ constexpr uint32_t d_col(int a) { return 8u * a * (a + 1); }
 constexpr uint32_t kTmemCols = 256;
 
 struct PrepArgs {
+    // TMA descriptors of q, k, v, g viewed as [tokens][H][128] bf16 with a box of
+    // 64 tokens x 1 head x 128 channels (one 16 KB row-major tile per copy)
+    CUtensorMap tm_q, tm_k, tm_v, tm_g;
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;
@@ -152,7 +156,9 @@ struct PrepShared {
     float sBeta[kChunk];
     float sTot[2][kDim];  // product of each half's alphas
     float sQf[2][kDim];   // prod_{s=32}^{39} and prod_{s=32}^{55} alpha_s
-    uint64_t bar;
+    uint64_t bar;       // MMA completion
+    uint64_t bar_g;     // g tile landed
+    uint64_t bar_qkv;   // q, k, v tiles landed
     uint32_t tmem_base;
     int s_abort;
 };
@@ -161,8 +167,65 @@ struct PrepShared {
 __device__ __forceinline__ void sub_sync(uint32_t bar_id) {
     asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kThreads) : "memory");
 }
+// One TMA tile copy (box of the tensor map at coordinates {x, y, z}) into shared
+// memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3, %4}], [%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
 __device__ __forceinline__ void st_release_gpu(int* p, int v) {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Off-diagonal blocks of T = (I + A)^-1 at block distance D (16 x 16 blocks,
+// a = b + D):  X_ab = sum_{c=b}^{a-1} A_ac T_cb,  T_ab = -T_aa X_ab.  Each of
+// the first (4 - D) * 64 threads computes a 2 x 2 tile (rows r, r+1; columns
+// c, c+1) of one block; the trip counts are compile-time constants.
+template <int D>
+__device__ __forceinline__ void level_products(const float* sAT, float* sT, float* sX, int tid,
+                                               uint32_t bar_id) {
+    constexpr int kItems = (4 - D) * 64;
+    const int b = tid >> 6, r = ((tid >> 3) & 7) * 2, c = (tid & 7) * 2;
+    const int a = b + D;
+    if (tid < kItems) {
+        float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+        const float* ap = sAT + 16 * b * kStr + 16 * a + r;
+        const float* tp = sT + 16 * b * kStr + 16 * b + c;
+#pragma unroll 8
+        for (int l = 0; l < 16 * D; ++l) {
+            const float2 av = *reinterpret_cast<const float2*>(ap + l * kStr);
+            const float2 tv = *reinterpret_cast<const float2*>(tp + l * kStr);
+            x00 = fmaf(av.x, tv.x, x00);
+            x01 = fmaf(av.x, tv.y, x01);
+            x10 = fmaf(av.y, tv.x, x10);
+            x11 = fmaf(av.y, tv.y, x11);
+        }
+        *reinterpret_cast<float2*>(sX + b * 256 + r * 16 + c) = make_float2(x00, x01);
+        *reinterpret_cast<float2*>(sX + b * 256 + (r + 1) * 16 + c) = make_float2(x10, x11);
+    }
+    sub_sync(bar_id);
+    if (tid < kItems) {
+        float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+        const float* t0p = sT + (16 * a + r) * kStr + 16 * a;
+#pragma unroll 8
+        for (int l = 0; l < 16; ++l) {
+            const float t0v = t0p[l];
+            const float t1v = t0p[kStr + l];
+            const float2 xv = *reinterpret_cast<const float2*>(sX + b * 256 + l * 16 + c);
+            y00 = fmaf(t0v, xv.x, y00);
+            y01 = fmaf(t0v, xv.y, y01);
+            y10 = fmaf(t1v, xv.x, y10);
+            y11 = fmaf(t1v, xv.y, y11);
+        }
+        *reinterpret_cast<float2*>(sT + (16 * a + r) * kStr + 16 * b + c) = make_float2(-y00, -y01);
+        *reinterpret_cast<float2*>(sT + (16 * a + r + 1) * kStr + 16 * b + c) =
+            make_float2(-y10, -y11);
+    }
+    sub_sync(bar_id);
 }
 
 // One chunk-kernel worker: `kThreads` threads (thread index `tid`), the
@@ -191,26 +254,19 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     const int half = tid >> 7;
     const int t0 = 32 * half;  // first token of this thread's half
 
-    // Issue the asynchronous copies of one item's q, k, v, g tiles (g in its
-    // own cp.async group, so the gate can start before q, k, v land) and set
-    // its beta.
+    // Issue the tile copies of one item's q, k, v, g (g on its own barrier, so
+    // the gate can start before q, k, v land) and set its beta.  Rows past the
+    // end of the tensor read as zeros; rows past the chunk's length (the next
+    // sequence's tokens) are zeroed after landing.
     auto stage = [&](const ChunkInfo& c, int hh, float beta_t) {
-        const __nv_bfloat16* srcs[4] = {P.g, P.q, P.k, P.v};
-        const uint32_t dsts[4] = {kSmG, kSmQ, kSmK, kSmV};
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int e = tid + kThreads * it;
-                const int row = e >> 4, col = e & 15;
-                const bool ok = row < c.len;
-                const __nv_bfloat16* src =
-                    srcs[x] + ((size_t)(ok ? c.tok0 + row : c.tok0) * H + hh) * kDim + col * 8;
-                cp_async16_zfill(sm + dsts[x] + row * 256 + col * 16, src, ok);
-            }
-            if (x == 0) cp_async_commit();
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&S.bar_g, kChunk * kDim * 2);
+            tma_load_3d(sm + kSmG, &P.tm_g, 0, hh, c.tok0, &S.bar_g);
+            mbar_arrive_expect_tx(&S.bar_qkv, 3 * kChunk * kDim * 2);
+            tma_load_3d(sm + kSmQ, &P.tm_q, 0, hh, c.tok0, &S.bar_qkv);
+            tma_load_3d(sm + kSmK, &P.tm_k, 0, hh, c.tok0, &S.bar_qkv);
+            tma_load_3d(sm + kSmV, &P.tm_v, 0, hh, c.tok0, &S.bar_qkv);
         }
-        cp_async_commit();
         if (tid < kChunk) S.sBeta[tid] = beta_t;
     };
     auto load_beta = [&](const ChunkInfo& c, int hh) -> float {
@@ -223,6 +279,8 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     }
     if (tid == 0) {
         mbar_init(&S.bar, 1);
+        mbar_init(&S.bar_g, 1);
+        mbar_init(&S.bar_qkv, 1);
         mbar_fence_init();
         S.s_abort = 0;
     }
@@ -236,6 +294,8 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     sub_sync(bar_id);
     tc_fence_after();
     const uint32_t tbase = S.tmem_base;
+    uint32_t tph = 0;       // phase of bar_g / bar_qkv for the current item
+    bool pending = true;    // an issued staging not yet waited for
 
     for (;;) {
     const int len = ci.len;
@@ -248,8 +308,12 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     const ChunkInfo ci_n = P.info[chunk_n];
     const float dtb_n = P.dt_bias[h_n * kDim + ch];
     const float alog_n = P.A_log[h_n];
-    cp_async_wait_group<1>();  // this thread's g copies
+    if (!mbar_wait(&S.bar_g, tph)) {
+        atomicOr(P.status, kStatusTimeout);
+        S.s_abort = 1;
+    }
     sub_sync(bar_id);
+    if (S.s_abort) break;
 
     // ---------------------------------------------------------------- gate (32 tokens)
     float al[32];
@@ -274,8 +338,22 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         }
         S.sTot[half][ch] = prod;
     }
-    cp_async_wait_group<0>();  // q, k, v
+    if (!mbar_wait(&S.bar_qkv, tph)) {
+        atomicOr(P.status, kStatusTimeout);
+        S.s_abort = 1;
+    }
+    pending = false;
+    if (len < kChunk) {
+        // zero the rows of tokens past the chunk's end in the q, k, v tiles
+        for (int e = tid; e < 3 * kChunk * 16; e += kThreads) {
+            const int tile = e / (kChunk * 16), r = (e / 16) % kChunk, piece = e & 15;
+            if (r >= len)
+                *reinterpret_cast<uint4*>(sm + tile * 16384 + r * 256 + piece * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
     sub_sync(bar_id);           // q, k, v, S.sTot, S.sQf visible
+    if (S.s_abort) break;
     uint32_t qp[16], kp[16];
 #pragma unroll
     for (int u = 0; u < 32; u += 2) {
@@ -540,49 +618,10 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
             for (int i = 0; i < 16; ++i) sT[(o + i) * kStr + o + j] = tc[i];
         }
         sub_sync(bar_id);
-        // off-diagonal blocks, one diagonal distance d at a time:
-        //   X_ab = sum_{c=b}^{a-1} A_ac T_cb ;  T_ab = -T_aa X_ab   (a = b + d)
-        // each thread computes a 2 x 2 tile (rows r, r+1; columns c, c+1)
-#pragma unroll
-        for (int d = 1; d < 4; ++d) {
-            const int nitems = (4 - d) * 64;
-            if (tid < nitems) {
-                const int b = tid >> 6, r = ((tid >> 3) & 7) * 2, c = (tid & 7) * 2;
-                const int a = b + d;
-                float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
-                for (int l = 16 * b; l < 16 * a; ++l) {
-                    const float2 av = *reinterpret_cast<const float2*>(sAT + l * kStr + 16 * a + r);
-                    const float2 tv = *reinterpret_cast<const float2*>(sT + l * kStr + 16 * b + c);
-                    x00 = fmaf(av.x, tv.x, x00);
-                    x01 = fmaf(av.x, tv.y, x01);
-                    x10 = fmaf(av.y, tv.x, x10);
-                    x11 = fmaf(av.y, tv.y, x11);
-                }
-                *reinterpret_cast<float2*>(sX + b * 256 + r * 16 + c) = make_float2(x00, x01);
-                *reinterpret_cast<float2*>(sX + b * 256 + (r + 1) * 16 + c) = make_float2(x10, x11);
-            }
-            sub_sync(bar_id);
-            if (tid < nitems) {
-                const int b = tid >> 6, r = ((tid >> 3) & 7) * 2, c = (tid & 7) * 2;
-                const int a = b + d;
-                float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
-#pragma unroll
-                for (int l = 0; l < 16; ++l) {
-                    const float t0v = sT[(16 * a + r) * kStr + 16 * a + l];
-                    const float t1v = sT[(16 * a + r + 1) * kStr + 16 * a + l];
-                    const float2 xv = *reinterpret_cast<const float2*>(sX + b * 256 + l * 16 + c);
-                    y00 = fmaf(t0v, xv.x, y00);
-                    y01 = fmaf(t0v, xv.y, y01);
-                    y10 = fmaf(t1v, xv.x, y10);
-                    y11 = fmaf(t1v, xv.y, y11);
-                }
-                *reinterpret_cast<float2*>(sT + (16 * a + r) * kStr + 16 * b + c) =
-                    make_float2(-y00, -y01);
-                *reinterpret_cast<float2*>(sT + (16 * a + r + 1) * kStr + 16 * b + c) =
-                    make_float2(-y10, -y11);
-            }
-            sub_sync(bar_id);
-        }
+        // off-diagonal blocks, one diagonal distance d at a time
+        level_products<1>(sAT, sT, sX, tid, bar_id);
+        level_products<2>(sAT, sT, sX, tid, bar_id);
+        level_products<3>(sAT, sT, sX, tid, bar_id);
         // T^T as MN-major B operand: element (n = t, k = s), k-groups 128 B, n-groups 1024 B
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
@@ -626,7 +665,11 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     // the staging area is free again: start the next item's copies
     float beta_n = 0.f;
     if (has_next && tid < kChunk) beta_n = load_beta(ci_n, h_n);
-    if (has_next) stage(ci_n, h_n, beta_n);
+    if (has_next) {
+        stage(ci_n, h_n, beta_n);
+        pending = true;
+        tph ^= 1u;
+    }
 
     // ---------------------------------------------------------------- W (warps 0-3), U^T (4-7)
     {
@@ -665,15 +708,49 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     tc_fence_before();
     }  // item loop
 
-    cp_async_wait_all();
+    if (pending) {
+        // an aborted worker waits (bounded) for its own tile copies before leaving
+        mbar_wait(&S.bar_g, tph);
+        mbar_wait(&S.bar_qkv, tph);
+    }
     tc_fence_before();
     sub_sync(bar_id);
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
 
-inline PrepArgs make_prep_args(const Problem& p, const Workspace& ws, int* status) {
-    PrepArgs a;
+// cuTensorMapEncodeTiled, fetched from the driver once.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+inline EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+// [tokens][H][128] bf16 -> tiles of 64 tokens x 1 head x 128 channels.
+inline bool encode_tile_map(CUtensorMap* m, const void* base, int64_t tokens, int H) {
+    const EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)H, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)kDim * 2, (cuuint64_t)H * kDim * 2};  // bytes
+    const cuuint32_t box[3] = {(cuuint32_t)kDim, 1u, (cuuint32_t)kChunk};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Arguments of the chunk kernel; false if a tensor map cannot be built.
+inline bool make_prep_args(const Problem& p, const Workspace& ws, int* status, PrepArgs& a) {
     a.q = reinterpret_cast<const __nv_bfloat16*>(p.q);
     a.k = reinterpret_cast<const __nv_bfloat16*>(p.k);
     a.v = reinterpret_cast<const __nv_bfloat16*>(p.v);
@@ -690,7 +767,10 @@ inline PrepArgs make_prep_args(const Problem& p, const Workspace& ws, int* statu
     a.info = ws.info;
     a.records = ws.records;
     a.status = status;
-    return a;
+    return encode_tile_map(&a.tm_q, p.q, p.total_tokens, p.H) &&
+           encode_tile_map(&a.tm_k, p.k, p.total_tokens, p.H) &&
+           encode_tile_map(&a.tm_v, p.v, p.total_tokens, p.H) &&
+           encode_tile_map(&a.tm_g, p.g, p.total_tokens, p.H);
 }
 
 }  // namespace prep
