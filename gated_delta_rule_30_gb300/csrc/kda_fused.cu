@@ -34,7 +34,7 @@ struct FusedArgs {
     int n_rec;   // blocks running a recurrence (one per pair)
 };
 
-__global__ void __launch_bounds__(kFusedThreads, 1) fused_kernel(const FusedArgs A) {
+__global__ void __launch_bounds__(kFusedThreads, 1) fused_kernel(const __grid_constant__ FusedArgs A) {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ prep::PrepShared ps[2];
     __shared__ recur_t::RecurTShared rs;
@@ -86,7 +86,7 @@ cudaError_t launch_fused(const Problem& p, const Workspace& ws, int* status, cud
     cudaError_t e = cudaMemsetAsync(ws.ready, 0, ready_bytes(p.max_chunks, p.H), st);
     if (e != cudaSuccess) return e;
     FusedArgs a;
-    a.p = prep::make_prep_args(p, ws, status);
+    if (!prep::make_prep_args(p, ws, status, a.p)) return cudaErrorInvalidValue;
     a.r = recur_t::make_recur_t_args(p, ws, status);
     a.ready = ws.ready;
     a.n_rec = p.N * p.H;

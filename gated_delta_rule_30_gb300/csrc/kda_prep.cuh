@@ -300,14 +300,10 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     for (;;) {
     const int len = ci.len;
     uint8_t* rec = P.records + ((size_t)chunk * H + h) * kRecBytes;
-    // the next item's chunk info and per-head parameters, loaded early
     const int next = item + item_stride;
     const bool has_next = next < n_items;
     const int chunk_n = has_next ? next / H : chunk;
     const int h_n = has_next ? next - chunk_n * H : h;
-    const ChunkInfo ci_n = P.info[chunk_n];
-    const float dtb_n = P.dt_bias[h_n * kDim + ch];
-    const float alog_n = P.A_log[h_n];
     if (!mbar_wait(&S.bar_g, tph)) {
         atomicOr(P.status, kStatusTimeout);
         S.s_abort = 1;
@@ -590,6 +586,12 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     }
     tc_fence_before();
     sub_sync(bar_id);
+
+    // the next item's chunk info and per-head parameters, loaded here (the
+    // register-heavy phases are over) so they arrive long before the staging
+    const ChunkInfo ci_n = P.info[chunk_n];
+    const float dtb_n = P.dt_bias[h_n * kDim + ch];
+    const float alog_n = P.A_log[h_n];
 
     // ---------------------------------------------------------------- T = (I + A)^-1
     {
