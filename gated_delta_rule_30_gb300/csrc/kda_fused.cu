@@ -43,12 +43,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_kernel(const __grid_co
         if ((int)threadIdx.x >= recur_t::kThreads) return;
         recur_t::recur_t_body(A.r, sm, rs, threadIdx.x, 1u, blockIdx.x, A.ready);
     } else {
-        const int sub = threadIdx.x / prep::kThreads;
         const int workers = 2 * ((int)gridDim.x - A.n_rec);
+        const int w0 = 2 * ((int)blockIdx.x - A.n_rec);
         // both workers share the SM's TMEM (256 columns each); neither gives up
-        // the allocation permit before the other has allocated
-        prep::prep_body(A.p, sm + sub * prep::kSmBytes, ps[sub], threadIdx.x % prep::kThreads,
-                        1u + sub, 2 * ((int)blockIdx.x - A.n_rec) + sub, workers, A.ready, false);
+        // the allocation permit before the other has allocated.  Each worker's
+        // shared-memory area is a compile-time offset: with a run-time base the
+        // worker needs more registers and ran 5% slower.
+        if ((int)threadIdx.x < prep::kThreads)
+            prep::prep_body(A.p, sm, ps[0], threadIdx.x, 1u, w0, workers, A.ready, false);
+        else
+            prep::prep_body(A.p, sm + prep::kSmBytes, ps[1], threadIdx.x - prep::kThreads, 2u,
+                            w0 + 1, workers, A.ready, false);
     }
 }
 
