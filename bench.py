@@ -199,6 +199,24 @@ def oracle_sample(p, target_s, max_tokens=None, fixed=None):
                       f"fp64 C oracle, OpenMP over (sequence, head), {dt:.1f} s"}
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(x, world, device):
+    """The largest of each rank's x (replicas: the job takes as long as the slowest)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, seconds):
+    """Whole-job rate: every rank processes its own replica of the workload."""
+    return units_per_rank * world / seconds
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -309,10 +327,7 @@ def main():
     clk = clocks.stop()
     kda.device_status(dev)
     ms_total = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / args.steps
     # events: [0] before the schedule kernel, [1] after it, [2] after the chunk
     # kernel (fused path: after the fused kernel), [3] after the recurrence
@@ -350,10 +365,7 @@ def main():
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     hbm_peak, bf16_peak, peak_kind = peaks()
     dominant = max((k for k in names if k != "schedule"), key=lambda k: stage_avg[k])
@@ -371,7 +383,7 @@ def main():
             traffic = tr.get("bytes_per_launch")
 
     line = {
-        "metric": METRIC, "value": head_tokens * world / (ms_step * 1e-3), "unit": UNIT,
+        "metric": METRIC, "value": job_throughput(head_tokens, world, ms_step * 1e-3), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
@@ -384,7 +396,7 @@ def main():
                      "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
                      "peak_kind": peak_kind,
                      "note": "achieved = counted bytes of the whole pass / dominant kernel time"},
-        "e2e": {"value": head_tokens * world / (e2e_ms * 1e-3), "unit": UNIT,
+        "e2e": {"value": job_throughput(head_tokens, world, e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": len(names) * args.steps,
         "clocks": clk,
