@@ -347,24 +347,61 @@ def main():
     h2d = sum(host[k].numel() * host[k].element_size() for k in in_keys)
     d2h = out.numel() * out.element_size() + (0 if hT is None else hT.numel() * hT.element_size())
 
-    def e2e_step():
-        for k in in_keys:
-            d[k].copy_(host[k], non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
-        if hT is not None:
-            hT_h.copy_(hT, non_blocking=True)
+    # Pipelined like a serving loop: two device input sets, one copy stream per
+    # input tensor (parallel copy engines), a copy-out stream.  Every step still
+    # copies all of its inputs in from pinned host memory and reads its output
+    # (and final state) back; step i+1's copies overlap step i's compute.
+    bufs = [d, {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}]
+    outs = [out, torch.empty_like(out)]
+    hTs = [hT, None if hT is None else torch.empty_like(hT)]
+    wss = [ws, torch.empty_like(ws)]
+    s_in = [torch.cuda.Stream(dev) for _ in in_keys]
+    s_out = torch.cuda.Stream(dev)
+    ev_free = [torch.cuda.Event() for _ in range(2)]   # compute on buffer set b finished
+    ev_read = [torch.cuda.Event() for _ in range(2)]   # output b read back to the host
+    for e in ev_free + ev_read:
+        e.record(stream)
 
-    e2e_step()
+    def e2e_step(i):
+        b = i & 1
+        landed = []
+        for j, k in enumerate(in_keys):
+            s_in[j].wait_event(ev_free[b])
+            with torch.cuda.stream(s_in[j]):
+                bufs[b][k].copy_(host[k], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(s_in[j])
+            landed.append(e)
+        for e in landed:
+            stream.wait_event(e)
+        stream.wait_event(ev_read[b])
+        x = bufs[b]
+        kda.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], outs[b], x["A_log"],
+                x["dt_bias"], x["lower_bound"], initial_state=x["initial_state"],
+                final_state=hTs[b], cu_seqlens=x["cu_seqlens"], workspace=wss[b])
+        ev_free[b].record(stream)
+        s_out.wait_event(ev_free[b])
+        with torch.cuda.stream(s_out):
+            out_h.copy_(outs[b], non_blocking=True)
+            if hT is not None:
+                hT_h.copy_(hTs[b], non_blocking=True)
+            ev_read[b].record(s_out)
+
+    for i in range(2):
+        e2e_step(i)
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    for st_ in s_in + [s_out]:
+        st_.wait_event(e0)
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    stream.wait_event(ev_read[(args.e2e_steps - 1) & 1])
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    kda.device_status(dev)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     hbm_peak, bf16_peak, peak_kind = peaks()
@@ -397,7 +434,9 @@ def main():
                      "peak_kind": peak_kind,
                      "note": "achieved = counted bytes of the whole pass / dominant kernel time"},
         "e2e": {"value": job_throughput(head_tokens, world, e2e_ms * 1e-3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "note": "pinned host buffers; copies of step i+1 overlap step i (two device "
+                        "input sets, one copy stream per input tensor)"},
         "gpu_launches": len(names) * args.steps,
         "clocks": clk,
     }
