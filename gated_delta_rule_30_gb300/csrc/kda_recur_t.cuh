@@ -105,9 +105,15 @@ __device__ __forceinline__ void state_st16(void* p, size_t base, const uint32_t 
     }
 }
 
-// Barrier over the kThreads threads of the recurrence block.
+// The barrier after the initial state load uses id bar_all + kBarStateOffset.
+constexpr uint32_t kBarStateOffset = 4;
+// Barrier over the kThreads threads of the recurrence block (and its
+// non-waiting arrival).
 __device__ __forceinline__ void all_sync(uint32_t bar_id) {
     asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kThreads) : "memory");
+}
+__device__ __forceinline__ void all_arrive(uint32_t bar_id) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(bar_id), "n"(kThreads) : "memory");
 }
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
     int v;
@@ -162,8 +168,8 @@ __device__ __forceinline__ void tmem_st8(uint32_t ta, const uint32_t (&r)[8]) {
 
 // The recurrence of (sequence, head) pair `pair` on kThreads threads (thread
 // index `tid`), with the shared-memory area `sm` (kSmemBytes, 1024-byte
-// aligned) and the small state `S`, synchronised by named barrier `bar_all`
-// (mbarriers elsewhere).  With `ready` non-null the record
+// aligned) and the small state `S`, synchronised by named barriers `bar_all`
+// and bar_all + kBarStateOffset (mbarriers elsewhere).  With `ready` non-null the record
 // of (chunk c, head h) is copied only once ready[c * H + h] is set.
 __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, RecurTShared& S,
                                              const int tid, const uint32_t bar_all,
@@ -231,7 +237,7 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
         }
         tmem_wait_st();
         tc_fence_before();
-        all_sync(bar_all);
+        all_sync(bar_all + kBarStateOffset);
         tc_fence_after();
 
         int i = 0;
@@ -332,8 +338,15 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
             }
         }
     } else {
+        // matches the chain warps' barrier after the initial state; the producer
+        // only arrives (it touches no TMEM), so the first record copies overlap
+        // the state load
+        // (its own barrier id: the producer may reach the final barrier first)
         tc_fence_before();
-        all_sync(bar_all);  // matches the epilogue warps' barrier after the initial state
+        if (warp == kWarpProducer)
+            all_arrive(bar_all + kBarStateOffset);
+        else
+            all_sync(bar_all + kBarStateOffset);
         tc_fence_after();
         if (warp == kWarpProducer) {
             // ---------------------------------------------------- producer
