@@ -186,6 +186,21 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
     const int c_begin = P.chunk_off[n];
     const int nchunks = P.chunk_off[n + 1] - c_begin;
     const int warp = tid >> 5, lane = tid & 31;
+    const size_t state_base = ((size_t)n * H + h) * kDim * kDim;
+    // The chain warps issue their initial-state loads first, so the DRAM
+    // latency overlaps the TMEM allocation and barrier set-up.  Thread (q, hc)
+    // holds S^T[v][k] = h0[k][v] for v = 32 q + lane and its 64 k.
+    uint32_t st0[64];
+    if (warp < kEpiWarps) {
+        const size_t b0 = state_base + (size_t)(64 * (warp >> 2)) * kDim + 32 * (warp & 3) + lane;
+        if (P.h0_dtype == KDA_DTYPE_FP32)
+            state_ld64<float>(P.h0, b0, st0);
+        else if (P.h0_dtype == KDA_DTYPE_BF16)
+            state_ld64<__nv_bfloat16>(P.h0, b0, st0);
+        else
+#pragma unroll
+            for (int j = 0; j < 64; ++j) st0[j] = 0u;
+    }
 
     if (warp == 0) {
         tmem_alloc(&S.tmem_base, kTmemCols);
@@ -212,29 +227,17 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
     all_sync(bar_all);
     tc_fence_after();
     const uint32_t tbase = S.tmem_base;
-    const size_t state_base = ((size_t)n * H + h) * kDim * kDim;
 
     if (warp < kEpiWarps) {
         // -------------------------------------------------------- epilogue warps
         const int q = warp & 3, hc = warp >> 2;
         const int v = 32 * q + lane;  // value channel = TMEM lane
         const uint32_t lane_base = taddr(tbase, 32u * q, 0);
-        // initial state, transposed: S^T[v][k] = h0[k][v] for this warp's 64 k
-        {
-            uint32_t r[64];
-            const size_t b0 = state_base + (size_t)(64 * hc) * kDim + v;
-            if (P.h0_dtype == KDA_DTYPE_FP32)
-                state_ld64<float>(P.h0, b0, r);
-            else if (P.h0_dtype == KDA_DTYPE_BF16)
-                state_ld64<__nv_bfloat16>(P.h0, b0, r);
-            else
+        // initial state (loaded above) to TMEM
 #pragma unroll
-                for (int j = 0; j < 64; ++j) r[j] = 0u;
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16)
-                tmem_st16(lane_base + kColS + 64 * hc + c0,
-                          *reinterpret_cast<const uint32_t(*)[16]>(r + c0));
-        }
+        for (int c0 = 0; c0 < 64; c0 += 16)
+            tmem_st16(lane_base + kColS + 64 * hc + c0,
+                      *reinterpret_cast<const uint32_t(*)[16]>(st0 + c0));
         tmem_wait_st();
         tc_fence_before();
         all_sync(bar_all + kBarStateOffset);
