@@ -229,6 +229,25 @@ def test_fused_matches_two_kernel_path(kda_lib, recur_kernel):
         assert torch.equal(o1, o3) and torch.equal(h1, h3)
 
 
+def test_automatic_path_choice(kda_lib, recur_kernel):
+    """kda_last_path reports the path automatic selection took: the fused launch
+    for few long sequences, the transposed recurrence when the pairs cover at
+    least half the SMs, the value-sliced one in between."""
+    if recur_kernel != "sliced":
+        pytest.skip("run once")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    kda_lib.set_recurrence_kernel("auto")
+    try:
+        cases = [(custom(T=1024, H=2, seed=3), "fused"),                    # 2 pairs x 16 chunks
+                 (make("state_io", n_seqs=sms, H=1), "transposed"),        # sms pairs, short
+                 (custom(lens=[100] * ((sms + 1) // 2 - 1), H=1, seed=4), "sliced")]
+        for p, want in cases:
+            run_gpu(p)
+            assert kda_lib.last_path() == want, (p["N"] * p["H"], want, kda_lib.last_path())
+    finally:
+        kda_lib.set_recurrence_kernel(recur_kernel)
+
+
 def test_malformed_cu_seqlens_reported(kda_lib):
     import gated_delta_rule_30_gb300 as kda
     p = custom(lens=[10, 20, 30], H=2, state=None, seed=1)
