@@ -52,8 +52,12 @@ def test_noalloc_matches_allocating_entry_twice(kda_lib):
     cases = [inputs.Workload("noalloc a", 1, None, 4, 51, lens=(70, 5, 129),
                              state_dtype=torch.float32),
              inputs.Workload("noalloc b", 1, None, 2, 52, lens=(33, 64),
-                             state_dtype=torch.bfloat16)]
-    for w in cases:  # two calls in a row; the second sees the first one's leftovers
+                             state_dtype=torch.bfloat16),
+             # few long sequences: the automatic choice is the fused launch, whose
+             # ready flags live in the same area
+             inputs.Workload("noalloc c", 1, None, 2, 53, lens=(1024, 700),
+                             state_dtype=torch.float32)]
+    for w in cases:  # calls in a row; each sees the previous one's leftovers
         p = inputs.make(w)
         ref_out, ref_hT = run_gpu(p)
         out, hT = _run_noalloc(kda_lib, p)
