@@ -84,6 +84,7 @@ KERNEL_SOURCES = {
     "recurrence/sliced": ("kda_recur.cu",),
     "recurrence/transposed": ("kda_recur_t.cu", "kda_recur_t.cuh"),
     "fused": ("kda_fused.cu", "kda_prep.cuh", "kda_recur_t.cuh"),
+    "decode": ("kda_decode.cu",),
 }
 
 
@@ -331,7 +332,9 @@ def main():
     ms_step = ms_total / args.steps
     # events: [0] before the schedule kernel, [1] after it, [2] after the chunk
     # kernel (fused path: after the fused kernel), [3] after the recurrence
-    names = ("schedule", "fused") if path == "fused" else ("schedule", "chunk", "recurrence")
+    # (single-token path: [0] before and [1] after its one kernel)
+    names = {"fused": ("schedule", "fused"), "decode": ("decode",)}.get(
+        path, ("schedule", "chunk", "recurrence"))
     stage_ms = {k: [] for k in names}
     for row in evs:
         for j, k in enumerate(names):

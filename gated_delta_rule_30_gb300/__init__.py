@@ -224,11 +224,12 @@ def set_recurrence_kernel(kind: str = "auto"):
     _check(lib().kda_set_recurrence_kernel(RECURRENCE_KERNELS[kind]))
 
 
-PATHS = {1: "sliced", 2: "transposed", 3: "fused"}
+PATHS = {1: "sliced", 2: "transposed", 3: "fused", 4: "decode"}
 
 
 def last_path():
-    """How this thread's last forward pass ran: "sliced", "transposed", "fused" (None before any)."""
+    """How this thread's last forward pass ran: "sliced", "transposed", "fused" or "decode"
+    (None before any)."""
     return PATHS.get(lib().kda_last_path())
 
 

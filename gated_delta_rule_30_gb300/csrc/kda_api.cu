@@ -266,6 +266,16 @@ kda_status_t run(const Problem& p, void* workspace, size_t workspace_size, cudaS
     if (p.N == 0) return KDA_OK;
     int* status = device_status_ptr();
     if (!status) return KDA_ERR_CUDA;
+    if (g_recur_kind == 0 && decode_applies(p)) {
+        // one token per sequence: a single pass over the states, no chunk records
+        stage_mark(0, st);
+        cudaError_t e = launch_decode(p, status, st);
+        stage_mark(1, st);
+        stage_mark(2, st);
+        stage_mark(3, st);
+        g_last_path = 4;
+        return e == cudaSuccess ? KDA_OK : cuda_error(e, "kernel launch");
+    }
     const size_t need = workspace_bytes(p.max_chunks, p.N, p.H);
     void* ws_ptr = workspace;
     bool owned = false;

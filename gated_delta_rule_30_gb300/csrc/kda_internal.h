@@ -102,6 +102,10 @@ constexpr int kStatusTimeout = 2;
 // Kernel launchers (kda_prep.cu, kda_recur.cu, kda_recur_t.cu, kda_api.cu).
 cudaError_t launch_schedule(const Problem& p, const Workspace& ws, int* status, cudaStream_t st);
 cudaError_t launch_prep(const Problem& p, const Workspace& ws, int* status, cudaStream_t st);
+// Single-token step (kda_decode.cu): T = 1 without cu_seqlens, no workspace.
+bool decode_applies(const Problem& p);
+cudaError_t launch_decode(const Problem& p, int* status, cudaStream_t st);
+
 // Fused launch (kda_fused.cu): chunk kernel and transposed recurrence in one
 // cooperative kernel.  fused_eligible says whether this device and problem
 // can take it (forced: the caller asked for it explicitly).

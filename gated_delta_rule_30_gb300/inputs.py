@@ -58,6 +58,9 @@ WORKLOADS = {
     "state_io": Workload("state_io: 1024 seqs U[1,128] H=32, fp32 state", 1, None, 32, 4,
                          n_seqs=1024, len_range=(1, 128), state_dtype=torch.float32),
 }
+# single-token step (one token per sequence with a state, as in decoding)
+WORKLOADS["decode"] = Workload("decode: B=1024 T=1 H=32, fp32 state", 1024, 1, 32, 5,
+                               state_dtype=torch.float32)
 # smaller instance of long_context used for profiler captures (inputs still exceed L2)
 WORKLOADS["long_context_8k"] = Workload("long_context_8k: B=1 T=8192 H=32, fp32 state", 1, 8192,
                                         32, 3, state_dtype=torch.float32)

@@ -164,7 +164,9 @@ const char* kda_last_error_message(void);
  * kda_fwd_ws / kda_fwd_noalloc call with a non-empty problem ran (no
  * counterpart on the pages; for benchmarks and diagnostics): 1 = chunk kernel
  * then value-sliced recurrence, 2 = chunk kernel then transposed recurrence,
- * 3 = the fused cooperative launch; 0 before any such call.
+ * 3 = the fused cooperative launch, 4 = the single-token step (T = 1 without
+ * cu_seqlens, chosen automatically: one pass over the states, the workspace
+ * is not used); 0 before any such call.
  */
 int kda_last_path(void);
 
@@ -187,11 +189,13 @@ kda_status_t kda_set_stage_events(void* const* events, int32_t count);
  * recurrence runs (no counterpart on the pages; every choice computes the same
  * operation to the same tolerance).  kind = 0 (default): chosen per call from
  * the number of (sequence, head) pairs, the chunks per sequence and the SM
- * count; 1: the value-sliced kernel (state slices of 32..128 value channels,
- * one CTA each); 2: the transposed kernel (one CTA per (sequence, head), state
- * held as S^T); 3: the fused launch (chunk kernel and transposed recurrence in
- * one cooperative kernel, overlapping; used only when the pairs leave at
- * least one SM for the chunk kernel, else kind 2 runs).  Process-wide,
+ * count, with single-token problems (T = 1, no cu_seqlens) taking the
+ * single-token step instead of the chunked path; 1: the value-sliced kernel
+ * (state slices of 32..128 value channels, one CTA each); 2: the transposed
+ * kernel (one CTA per (sequence, head), state held as S^T); 3: the fused
+ * launch (chunk kernel and transposed recurrence in one cooperative kernel,
+ * overlapping; used only when the pairs leave at least one SM for the chunk
+ * kernel, else kind 2 runs).  Process-wide,
  * applies to later calls; not thread-safe.  Any other kind returns
  * KDA_ERR_INVALID_ARGUMENT.
  */
