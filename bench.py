@@ -85,7 +85,12 @@ KERNEL_SOURCES = {
     "recurrence/transposed": ("kda_recur_t.cu", "kda_recur_t.cuh"),
     "fused": ("kda_fused.cu", "kda_prep.cuh", "kda_recur_t.cuh"),
     "decode": ("kda_decode.cu",),
+    "recurrence/segmented": ("kda_recur.cu",),
+    "maps": ("kda_recur.cu", "kda_segmented.cu"),
+    "scan": ("kda_segmented.cu",),
 }
+# kernels one forward pass launches, per path
+LAUNCHES = {"sliced": 3, "transposed": 3, "fused": 2, "decode": 1, "segmented": 6}
 
 
 def kernel_source_hash(kernel):
@@ -230,6 +235,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="auto",
+                    choices=["auto", "sliced", "transposed", "fused", "segmented"],
+                    help="recurrence selection (default: the library's automatic choice)")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
 
@@ -277,6 +285,7 @@ def main():
     kbuild.build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    kda.set_recurrence_kernel(args.path)  # before the workspace size query
 
     p = inputs.make(w)
     head_tokens, flops, alg_bytes = counted_work(p)
@@ -301,7 +310,7 @@ def main():
 
     # stage events: per-kernel durations measured on the launch stream
     n_ev = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_ev)]
     for row in evs:
         for e in row:
             e.record(stream)
@@ -332,8 +341,10 @@ def main():
     ms_step = ms_total / args.steps
     # events: [0] before the schedule kernel, [1] after it, [2] after the chunk
     # kernel (fused path: after the fused kernel), [3] after the recurrence
-    # (single-token path: [0] before and [1] after its one kernel)
-    names = {"fused": ("schedule", "fused"), "decode": ("decode",)}.get(
+    # (single-token path: [0] before and [1] after its one kernel; segmented
+    # path: [3] after the map pass, [4] after the scan, [5] after the recurrence)
+    names = {"fused": ("schedule", "fused"), "decode": ("decode",),
+             "segmented": ("schedule", "chunk", "maps", "scan", "recurrence")}.get(
         path, ("schedule", "chunk", "recurrence"))
     stage_ms = {k: [] for k in names}
     for row in evs:
@@ -440,7 +451,7 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "note": "pinned host buffers; copies of step i+1 overlap step i (two device "
                         "input sets, one copy stream per input tensor)"},
-        "gpu_launches": len(names) * args.steps,
+        "gpu_launches": LAUNCHES[path] * args.steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

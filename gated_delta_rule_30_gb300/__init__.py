@@ -212,33 +212,37 @@ def device_status(device=None):
         _check(lib().kda_device_status(_stream_ptr(dev)))
 
 
-RECURRENCE_KERNELS = {"auto": 0, "sliced": 1, "transposed": 2, "fused": 3}
+RECURRENCE_KERNELS = {"auto": 0, "sliced": 1, "transposed": 2, "fused": 3, "segmented": 4}
 
 
 def set_recurrence_kernel(kind: str = "auto"):
-    """Choose the recurrence kernel for later calls: "auto", "sliced", "transposed" or "fused"
+    """Choose the recurrence kernel for later calls: "auto", "sliced", "transposed", "fused"
     (chunk kernel and transposed recurrence in one cooperative launch; falls back to the
-    two-kernel path when the problem has too many (sequence, head) pairs for it)."""
+    two-kernel path when the problem has too many (sequence, head) pairs for it) or
+    "segmented" (each sequence split into segments whose state maps are scanned, then all
+    segments run at once).  The workspace size depends on this choice: query
+    ``workspace_size`` after setting it."""
     if kind not in RECURRENCE_KERNELS:
         raise ValueError(f"kind must be one of {sorted(RECURRENCE_KERNELS)}")
     _check(lib().kda_set_recurrence_kernel(RECURRENCE_KERNELS[kind]))
 
 
-PATHS = {1: "sliced", 2: "transposed", 3: "fused", 4: "decode"}
+PATHS = {1: "sliced", 2: "transposed", 3: "fused", 4: "decode", 5: "segmented"}
 
 
 def last_path():
-    """How this thread's last forward pass ran: "sliced", "transposed", "fused" or "decode"
-    (None before any)."""
+    """How this thread's last forward pass ran: "sliced", "transposed", "fused", "decode" or
+    "segmented" (None before any)."""
     return PATHS.get(lib().kda_last_path())
 
 
 def set_stage_events(events):
-    """Record 4 CUDA events around the library's kernels in later calls (None: off).
+    """Record 4 or 6 CUDA events around the library's kernels in later calls (None: off).
 
-    ``events``: four ``torch.cuda.Event(enable_timing=True)`` objects; they mark
+    ``events``: ``torch.cuda.Event(enable_timing=True)`` objects; they mark
     before schedule / after schedule / after the chunk kernel / after the
-    recurrence kernel on the call's stream.
+    recurrence kernel on the call's stream (segmented path: after the chunk
+    kernel / after the map pass / after the scan / after the recurrence).
     """
     L = lib()
     if events is None:
@@ -247,8 +251,9 @@ def set_stage_events(events):
     for e in events:
         if e.cuda_event == 0:
             raise ValueError("events must be created (record them once) before use")
-    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
-    _check(L.kda_set_stage_events(arr, 4))
+    n = len(events)
+    arr = (ctypes.c_void_p * n)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(L.kda_set_stage_events(arr, n))
 
 
 def selftest_tcgen05(a, b, N, K):

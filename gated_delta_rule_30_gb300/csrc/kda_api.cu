@@ -61,13 +61,23 @@ namespace {
 constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 }  // namespace
 
-size_t workspace_bytes(int64_t max_chunks, int64_t N, int64_t H) {
+namespace {
+// segmented path: segment offsets, X and M^T per (segment, head), entering states
+size_t segment_area_bytes(int64_t N, int64_t H, int segs) {
+    if (segs <= 0) return 0;
+    const size_t nseg = (size_t)N * segs;
+    return align256((nseg + 1) * sizeof(int32_t)) + nseg * (size_t)H * 3 * kDim * kDim * sizeof(float);
+}
+}  // namespace
+
+size_t workspace_bytes(int64_t max_chunks, int64_t N, int64_t H, int segs) {
     return 256 + align256((size_t)(N + 1) * sizeof(int32_t)) +
            align256((size_t)max_chunks * sizeof(ChunkInfo)) +
-           (size_t)max_chunks * (size_t)H * kRecBytes + align256(ready_bytes(max_chunks, H));
+           (size_t)max_chunks * (size_t)H * kRecBytes + align256(ready_bytes(max_chunks, H)) +
+           segment_area_bytes(N, H, segs);
 }
 
-Workspace carve_workspace(void* base, int64_t max_chunks, int64_t N, int64_t H) {
+Workspace carve_workspace(void* base, int64_t max_chunks, int64_t N, int64_t H, int segs) {
     uint8_t* p = static_cast<uint8_t*>(base);
     Workspace w;
     w.flags = reinterpret_cast<int32_t*>(p);
@@ -79,6 +89,19 @@ Workspace carve_workspace(void* base, int64_t max_chunks, int64_t N, int64_t H) 
     w.records = p;
     p += (size_t)max_chunks * (size_t)H * kRecBytes;
     w.ready = reinterpret_cast<int32_t*>(p);
+    p += align256(ready_bytes(max_chunks, H));
+    w.segs = segs > 0 ? segs : 0;
+    w.seg_off = nullptr;
+    w.seg_maps = nullptr;
+    w.seg_start = nullptr;
+    if (w.segs > 0) {
+        const size_t nseg = (size_t)N * w.segs;
+        w.seg_off = reinterpret_cast<int32_t*>(p);
+        p += align256((nseg + 1) * sizeof(int32_t));
+        w.seg_maps = reinterpret_cast<float*>(p);
+        p += nseg * (size_t)H * 2 * kDim * kDim * sizeof(float);
+        w.seg_start = reinterpret_cast<float*>(p);
+    }
     return w;
 }
 
@@ -141,24 +164,32 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
         __syncthreads();
         const int excl = x - nc + (warp > 0 ? warp_sums[warp - 1] : 0);
         const int carry = s_carry;
-        if (n < N) {
-            const int first = carry + excl;
-            chunk_off[n] = first;
-            const int tok0 = cu ? cu[n] : n * T;
-            for (int c = 0; c < nc; ++c) {
-                ChunkInfo ci;
-                ci.tok0 = tok0 + c * kChunk;
-                ci.len = min(kChunk, len - c * kChunk);
-                info[first + c] = ci;
-            }
-        }
+        if (n < N) chunk_off[n] = carry + excl;
         __syncthreads();
         if (tid == 0) s_carry = carry + warp_sums[31];
         __syncthreads();
     }
+    const int total = s_carry;
     if (tid == 0) {
-        chunk_off[N] = s_carry;
-        flags[0] = (s_carry <= max_chunks) ? 1 : 0;
+        chunk_off[N] = total;
+        flags[0] = (total <= max_chunks) ? 1 : 0;
+    }
+    if (total > max_chunks) return;
+    // chunk table, one chunk per thread: chunk c belongs to the last sequence n
+    // with chunk_off[n] <= c (empty sequences share their successor's offset)
+    for (int c = tid; c < total; c += kSchedThreads) {
+        int lo = 0, hi = N - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (chunk_off[mid] <= c) lo = mid;
+            else hi = mid - 1;
+        }
+        const int j = c - chunk_off[lo];  // chunk index within sequence lo
+        const int len = cu ? cu[lo + 1] - cu[lo] : T;
+        ChunkInfo ci;
+        ci.tok0 = (cu ? cu[lo] : lo * T) + j * kChunk;
+        ci.len = min(kChunk, len - j * kChunk);
+        info[c] = ci;
     }
 }
 
@@ -254,12 +285,13 @@ kda_status_t build_problem(Problem& p, const void* q, const void* k, const void*
     return KDA_OK;
 }
 
-cudaEvent_t g_stage_events[4] = {nullptr, nullptr, nullptr, nullptr};
-bool g_stage_on = false;
-int g_recur_kind = 0;  // kda_set_recurrence_kernel
+constexpr int kMaxStageEvents = 6;
+cudaEvent_t g_stage_events[kMaxStageEvents] = {nullptr};
+int g_stage_count = 0;  // 0: off
+int g_recur_kind = 0;   // kda_set_recurrence_kernel
 
 void stage_mark(int i, cudaStream_t st) {
-    if (g_stage_on) cudaEventRecord(g_stage_events[i], st);
+    if (i < g_stage_count) cudaEventRecord(g_stage_events[i], st);
 }
 
 kda_status_t run(const Problem& p, void* workspace, size_t workspace_size, cudaStream_t st) {
@@ -276,7 +308,8 @@ kda_status_t run(const Problem& p, void* workspace, size_t workspace_size, cudaS
         g_last_path = 4;
         return e == cudaSuccess ? KDA_OK : cuda_error(e, "kernel launch");
     }
-    const size_t need = workspace_bytes(p.max_chunks, p.N, p.H);
+    const int segs = segment_count(p.N, p.H, p.max_chunks, g_recur_kind);
+    const size_t need = workspace_bytes(p.max_chunks, p.N, p.H, segs);
     void* ws_ptr = workspace;
     bool owned = false;
     if (!ws_ptr) {
@@ -289,9 +322,29 @@ kda_status_t run(const Problem& p, void* workspace, size_t workspace_size, cudaS
         if (reinterpret_cast<uintptr_t>(ws_ptr) & 255u)
             return set_error(KDA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
     }
-    const Workspace ws = carve_workspace(ws_ptr, p.max_chunks, p.N, p.H);
+    const Workspace ws = carve_workspace(ws_ptr, p.max_chunks, p.N, p.H, segs);
     stage_mark(0, st);
     cudaError_t e = launch_schedule(p, ws, status, st);
+    if (segs > 0) {
+        // few long sequences: segments scanned in parallel (kda_segmented.cu)
+        if (e == cudaSuccess) e = launch_seg_schedule(p, ws, st);
+        stage_mark(1, st);
+        if (e == cudaSuccess) e = launch_prep(p, ws, status, st);
+        stage_mark(2, st);
+        if (e == cudaSuccess) e = launch_seg_maps(p, ws, status, st);
+        stage_mark(3, st);
+        if (e == cudaSuccess) e = launch_seg_scan(p, ws, status, st);
+        stage_mark(4, st);
+        if (e == cudaSuccess) e = launch_seg_outputs(p, ws, status, st);
+        stage_mark(5, st);
+        g_last_path = 5;
+        kda_status_t rc = e == cudaSuccess ? KDA_OK : cuda_error(e, "kernel launch");
+        if (owned) {
+            cudaError_t f = cudaFreeAsync(ws_ptr, st);
+            if (f != cudaSuccess && rc == KDA_OK) rc = cuda_error(f, "cudaFreeAsync(workspace)");
+        }
+        return rc;
+    }
     stage_mark(1, st);
     // kind 3 asks for the fused launch; automatic selection takes it for few,
     // long sequences
@@ -377,7 +430,7 @@ extern "C" size_t kda_workspace_size(int32_t B, int32_t T, int32_t H, int32_t nu
     const int64_t N = has_cu_seqlens ? num_seqs : B;
     const int64_t total = (int64_t)B * T;
     const int64_t max_chunks = (total + (int64_t)(kChunk - 1) * N) / kChunk;
-    return workspace_bytes(max_chunks, N, H);
+    return workspace_bytes(max_chunks, N, H, segment_count(N, H, max_chunks, g_recur_kind));
 }
 
 extern "C" kda_status_t kda_device_status(void* stream) {
@@ -419,8 +472,8 @@ extern "C" int kda_abi_version(void) { return KDA_ABI_VERSION; }
 
 extern "C" kda_status_t kda_set_recurrence_kernel(int32_t kind) {
     clear_error();
-    if (kind < 0 || kind > 3)
-        return set_error(KDA_ERR_INVALID_ARGUMENT, "kind must be 0, 1, 2 or 3");
+    if (kind < 0 || kind > 4)
+        return set_error(KDA_ERR_INVALID_ARGUMENT, "kind must be 0, 1, 2, 3 or 4");
     g_recur_kind = kind;
     return KDA_OK;
 }
@@ -428,14 +481,14 @@ extern "C" kda_status_t kda_set_recurrence_kernel(int32_t kind) {
 extern "C" kda_status_t kda_set_stage_events(void* const* events, int32_t count) {
     clear_error();
     if (events == nullptr || count == 0) {
-        g_stage_on = false;
+        g_stage_count = 0;
         return KDA_OK;
     }
-    if (count != 4) return set_error(KDA_ERR_INVALID_ARGUMENT, "count must be 0 or 4");
-    for (int i = 0; i < 4; ++i) {
+    if (count != 4 && count != kMaxStageEvents)
+        return set_error(KDA_ERR_INVALID_ARGUMENT, "count must be 0, 4 or 6");
+    for (int i = 0; i < count; ++i)
         if (!events[i]) return set_error(KDA_ERR_INVALID_ARGUMENT, "null event");
-        g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
-    }
-    g_stage_on = true;
+    for (int i = 0; i < count; ++i) g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+    g_stage_count = count;
     return KDA_OK;
 }

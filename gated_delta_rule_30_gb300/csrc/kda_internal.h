@@ -62,6 +62,13 @@ struct Workspace {
     ChunkInfo* info;      // [max_chunks]
     uint8_t* records;     // [max_chunks][H][kRecBytes]
     int32_t* ready;       // [max_chunks][H] record-complete flags (fused launch only)
+    // segmented path only (segs > 0; see kda_segmented.cu): each sequence's
+    // chunks split into segs runs
+    int segs;             // segments per sequence (0: no segment area)
+    int32_t* seg_off;     // [N * segs + 1] chunk offsets of the segments
+    float* seg_maps;      // [N * segs][H][2][128][128]: X (state reached from zero, [k][v]),
+                          // then M^T (linear part of the segment's state map, [j][k])
+    float* seg_start;     // [N * segs][H][128][128]: state entering each segment, [k][v]
 };
 
 struct Problem {
@@ -86,8 +93,8 @@ struct Problem {
     int64_t max_chunks;
 };
 
-size_t workspace_bytes(int64_t max_chunks, int64_t N, int64_t H);
-Workspace carve_workspace(void* base, int64_t max_chunks, int64_t N, int64_t H);
+size_t workspace_bytes(int64_t max_chunks, int64_t N, int64_t H, int segs);
+Workspace carve_workspace(void* base, int64_t max_chunks, int64_t N, int64_t H, int segs);
 
 // Error reporting (thread-local message).
 kda_status_t set_error(kda_status_t s, const char* msg);
@@ -120,8 +127,24 @@ inline size_t ready_bytes(int64_t max_chunks, int64_t H) {
 int recur_choose(const Problem& p, int kind);
 cudaError_t launch_recur(const Problem& p, const Workspace& ws, int* status, cudaStream_t st,
                          int kind);
+// vs: value-slice width 32, 64 or 128 (0: chosen from the number of pairs)
 cudaError_t launch_recur_sliced(const Problem& p, const Workspace& ws, int* status,
-                                cudaStream_t st);
+                                cudaStream_t st, int vs = 0);
+// Segment maps (kda_recur.cu): for the N pseudo-sequences of p (the segments,
+// ws.chunk_off = their chunk offsets) writes X and M^T into ws.seg_maps.
+cudaError_t launch_recur_maps(const Problem& p, const Workspace& ws, int* status,
+                              cudaStream_t st);
+
+// Segmented path (kda_segmented.cu): split each sequence into segments, find
+// each segment's affine state map, scan them, then run the recurrence on all
+// segments at once.  segment_count gives the segments per sequence for the
+// recurrence selection `kind` (0 automatic, 4 forced; 0 = path not taken).
+int segment_count(int64_t N, int64_t H, int64_t max_chunks, int kind);
+cudaError_t launch_seg_schedule(const Problem& p, const Workspace& ws, cudaStream_t st);
+cudaError_t launch_seg_maps(const Problem& p, const Workspace& ws, int* status, cudaStream_t st);
+cudaError_t launch_seg_scan(const Problem& p, const Workspace& ws, int* status, cudaStream_t st);
+cudaError_t launch_seg_outputs(const Problem& p, const Workspace& ws, int* status,
+                               cudaStream_t st);
 cudaError_t launch_recur_transposed(const Problem& p, const Workspace& ws, int* status,
                                    cudaStream_t st);
 

@@ -28,6 +28,15 @@
 // the next snapshot is taken.  Every mbarrier wait is bounded; on timeout the
 // CTA records kStatusTimeout, stops, waits (bounded) for its own copies and
 // frees TMEM.
+//
+// Map mode (kMap, segmented path): the grid holds twice the slices of each
+// (segment, head).  Slices [0, 128/VS) start from a zero state and give X, the
+// state the segment reaches from zero; slices [128/VS, 256/VS) start from the
+// identity with U taken as zero (Delta = -X[0:64]) and give the linear part M
+// of the segment's state map, since each value column evolves by
+// s <- (Diag(gamma) - Ktilde^T W) s + Ktilde^T u.  No outputs are formed
+// (the output product and the output warps are skipped); the final slice is
+// stored as X [k][v] or as M^T [j][k].
 #include <cuda_runtime.h>
 
 #include <type_traits>
@@ -131,11 +140,12 @@ struct NoState {};
         break;                                             \
     }
 
-// H0 / HT: float, __nv_bfloat16 or NoState
-template <int VS, typename H0, typename HT>
+// H0 / HT: float, __nv_bfloat16 or NoState; kMap: map mode (H0 = NoState, HT = float)
+template <int VS, typename H0, typename HT, bool kMap = false>
 __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
     using L = RecurLayout<VS>;
     constexpr int kSlices = kDim / VS;
+    constexpr int kGridSlices = kMap ? 2 * kSlices : kSlices;
     extern __shared__ __align__(1024) uint8_t sm[];
     // full/empty: record ring; s_ready: snapshot written; mma1: X = [W;Q].S done;
     // d_ready: Delta written; mma2s: state update done; mma2o[b]: output update
@@ -152,8 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
     __syncthreads();
     if (s_abort) return;
     const int H = P.H;
-    const int slice = blockIdx.x % kSlices;
-    const int nh = blockIdx.x / kSlices;
+    const int gslice = blockIdx.x % kGridSlices;
+    const bool lin = kMap && gslice >= kSlices;  // map mode: this CTA evolves the identity
+    const int slice = lin ? gslice - kSlices : gslice;
+    const int nh = blockIdx.x / kGridSlices;
     const int h = nh % H;
     const int n = nh / H;
     const int v0 = slice * VS;
@@ -187,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
     tc_fence_after();
     const uint32_t tbase = tmem_base;
     const uint32_t tS = tbase;  // columns [0, VS); X[b] at [VS (1 + b), VS (2 + b))
-    const size_t state_base = ((size_t)n * H + h) * kDim * kDim;
+    const size_t state_base = (kMap ? (size_t)nh * 2 + (lin ? 1 : 0) : (size_t)nh) * kDim * kDim;
 
     // initial state -> TMEM (thread = key channel)
     if (warp < 4) {
@@ -195,7 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
 #pragma unroll
         for (int c0 = 0; c0 < VS; c0 += 16) {
             uint32_t r[16];
-            if constexpr (std::is_same<H0, NoState>::value) {
+            if constexpr (kMap) {
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    r[u] = (lin && ch == v0 + c0 + u) ? __float_as_uint(1.f) : 0u;
+            } else if constexpr (std::is_same<H0, NoState>::value) {
 #pragma unroll
                 for (int u = 0; u < 16; ++u) r[u] = 0u;
             } else {
@@ -285,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
             const uint32_t tX = tbase + VS * (1 + (i & 1));
             WAIT_OR_ABORT(&full[s], (uint32_t)((i / NS) & 1));
             // X[i % 2] still holds the outputs of chunk i - 2 until they are read
-            if (i >= 2) WAIT_OR_ABORT(&x_free[i & 1], (uint32_t)(((i - 2) >> 1) & 1));
+            if (!kMap && i >= 2) WAIT_OR_ABORT(&x_free[i & 1], (uint32_t)(((i - 2) >> 1) & 1));
             WAIT_OR_ABORT(&s_ready, ph);
             tc_fence_after();
             const uint64_t so = (uint64_t)s * kStageStep;
@@ -304,9 +320,11 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tS, dKT0 + so + 16u * kk, dd + 16u * kk, idesc2, 1u);
                 mma_commit(&mma2s);
+                // map mode: no output product; the stage is free once the state update has read it
+                if (kMap) mma_commit(&empty[s]);
             }
             __syncwarp();
-            issue_out(i);
+            if (!kMap) issue_out(i);
         }
     } else if (warp < 4) {
         // ------------------------------------------------------------ state / epilogue warps
@@ -349,7 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
                 uint32_t u_pk[VS / 2];  // U[row][c], two bf16 per register, read before waiting
 #pragma unroll
                 for (int c = 0; c < VS; c += 2)
-                    u_pk[c / 2] = (uint32_t)ut[c * 64 + row] | ((uint32_t)ut[(c + 1) * 64 + row] << 16);
+                    u_pk[c / 2] = lin ? 0u
+                                      : ((uint32_t)ut[c * 64 + row] |
+                                         ((uint32_t)ut[(c + 1) * 64 + row] << 16));
                 WAIT_OR_ABORT(&mma1, ph);
                 tc_fence_after();
                 const uint32_t tX = tbase + VS * (1 + (i & 1));
@@ -380,7 +400,22 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
             tc_fence_after();
         }
         if (!*((volatile int*)&s_abort)) {
-            if constexpr (!std::is_same<HT, NoState>::value) {
+            if constexpr (kMap) {
+                const int ch = row;
+#pragma unroll
+                for (int c0 = 0; c0 < VS; c0 += 16) {
+                    uint32_t r[16];
+                    tmem_load16(taddr(tS, 32u * warp, (uint32_t)c0), r);
+                    if (lin) {  // M^T[j][k]: a warp's 32 key channels are 32 consecutive words
+                        float* mt = reinterpret_cast<float*>(P.hT) + state_base;
+#pragma unroll
+                        for (int u = 0; u < 16; ++u)
+                            mt[(size_t)(v0 + c0 + u) * kDim + ch] = __uint_as_float(r[u]);
+                    } else {
+                        StateIO<float>::store16(P.hT, state_base + (size_t)ch * kDim + v0 + c0, r);
+                    }
+                }
+            } else if constexpr (!std::is_same<HT, NoState>::value) {
                 const int ch = row;
 #pragma unroll
                 for (int c0 = 0; c0 < VS; c0 += 16) {
@@ -390,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
                 }
             }
         }
-    } else {
+    } else if (!kMap) {
         // ------------------------------------------------------------ output warps
         // warps 6 and 7 (TMEM lane quarters 2 and 3: rows 64..127 of X) write
         // the outputs of chunk j from X[j % 2], then release that buffer
@@ -431,13 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
     if (warp == 0) tmem_dealloc(tbase, L::kTmemCols);
 }
 
-template <int VS, typename H0, typename HT>
+template <int VS, typename H0, typename HT, bool kMap = false>
 cudaError_t launch_recur_t(const Problem& p, const RecurArgs& a, cudaStream_t st) {
     using L = RecurLayout<VS>;
-    auto kern = recur_kernel<VS, H0, HT>;
+    auto kern = recur_kernel<VS, H0, HT, kMap>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
-    const long long blocks = (long long)p.N * p.H * (kDim / VS);
+    const long long blocks = (long long)p.N * p.H * (kDim / VS) * (kMap ? 2 : 1);
     kern<<<(unsigned)blocks, kThreads, L::kBytes, st>>>(a);
     return cudaGetLastError();
 }
@@ -472,9 +507,8 @@ int recur_slice_width(const Problem& p, int num_sms) {
     return 32;
 }
 
-cudaError_t launch_recur_sliced(const Problem& p, const Workspace& ws, int* status,
-                                cudaStream_t st) {
-    if (p.N == 0 || p.H == 0) return cudaSuccess;
+namespace {
+RecurArgs recur_args(const Problem& p, const Workspace& ws, int* status) {
     RecurArgs a;
     a.out = p.out;
     a.h0 = p.h0;
@@ -486,14 +520,36 @@ cudaError_t launch_recur_sliced(const Problem& p, const Workspace& ws, int* stat
     a.info = ws.info;
     a.records = ws.records;
     a.status = status;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    switch (recur_slice_width(p, sms)) {
+    return a;
+}
+}  // namespace
+
+cudaError_t launch_recur_sliced(const Problem& p, const Workspace& ws, int* status,
+                                cudaStream_t st, int vs) {
+    if (p.N == 0 || p.H == 0) return cudaSuccess;
+    const RecurArgs a = recur_args(p, ws, status);
+    if (vs == 0) {
+        int dev = 0, sms = 148;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        vs = recur_slice_width(p, sms);
+    }
+    switch (vs) {
         case 128: return launch_recur_vs<128>(p, a, st);
         case 64: return launch_recur_vs<64>(p, a, st);
         default: return launch_recur_vs<32>(p, a, st);
     }
+}
+
+cudaError_t launch_recur_maps(const Problem& p, const Workspace& ws, int* status,
+                              cudaStream_t st) {
+    if (p.N == 0 || p.H == 0) return cudaSuccess;
+    RecurArgs a = recur_args(p, ws, status);
+    a.out = nullptr;
+    a.h0 = nullptr;
+    a.hT = ws.seg_maps;
+    // one 128-wide slice for X and one for M per (segment, head)
+    return launch_recur_t<128, NoState, float, true>(p, a, st);
 }
 
 bool recur_prefers_transposed(const Problem& p, int num_sms) {

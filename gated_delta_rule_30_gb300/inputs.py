@@ -61,6 +61,9 @@ WORKLOADS = {
 # single-token step (one token per sequence with a state, as in decoding)
 WORKLOADS["decode"] = Workload("decode: B=1024 T=1 H=32, fp32 state", 1024, 1, 32, 5,
                                state_dtype=torch.float32)
+# long_context with its 32 heads split over 8 tensor-parallel GPUs: the 4 heads one GPU holds
+WORKLOADS["long_context_4h"] = Workload("long_context_4h: B=1 T=65536 H=4, fp32 state", 1, 65536,
+                                        4, 6, state_dtype=torch.float32)
 # smaller instance of long_context used for profiler captures (inputs still exceed L2)
 WORKLOADS["long_context_8k"] = Workload("long_context_8k: B=1 T=8192 H=32, fp32 state", 1, 8192,
                                         32, 3, state_dtype=torch.float32)

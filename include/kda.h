@@ -97,8 +97,10 @@ kda_status_t kda_fwd(const void* q, const void* k, const void* v, const void* g,
 
 /*
  * kda_workspace_size -- bytes of device scratch kda_fwd_ws needs for a
- * problem with these sizes (an upper bound that does not read cu_seqlens).
- * Returns 0 and sets the error message for invalid sizes.
+ * problem with these sizes (an upper bound that does not read cu_seqlens),
+ * for the recurrence selection in force (kda_set_recurrence_kernel: the
+ * segmented path needs room for its per-segment states, so query the size
+ * after choosing).  Returns 0 and sets the error message for invalid sizes.
  */
 size_t kda_workspace_size(int32_t B, int32_t T, int32_t H, int32_t num_seqs, int32_t has_cu_seqlens);
 
@@ -166,7 +168,8 @@ const char* kda_last_error_message(void);
  * then value-sliced recurrence, 2 = chunk kernel then transposed recurrence,
  * 3 = the fused cooperative launch, 4 = the single-token step (T = 1 without
  * cu_seqlens, chosen automatically: one pass over the states, the workspace
- * is not used); 0 before any such call.
+ * is not used), 5 = the segmented path (chunk kernel, per-segment state maps,
+ * scan, value-sliced recurrence over the segments); 0 before any such call.
  */
 int kda_last_path(void);
 
@@ -175,12 +178,16 @@ int kda_abi_version(void);
 
 /*
  * kda_set_stage_events -- timing hook (no counterpart on the pages).  With
- * count = 4, every later kda_fwd / kda_fwd_ws call on this process records
- * events[0] before its first kernel, events[1] after the chunk-schedule
- * kernel, events[2] after the chunk kernel and events[3] after the recurrence
- * kernel, all on the call's stream (events are cudaEvent_t created by the
- * caller and must outlive the calls).  count = 0 (or events = NULL) turns the
- * hook off.  Not thread-safe; intended for benchmarks.
+ * count = 4 or 6, every later kda_fwd / kda_fwd_ws call on this process
+ * records events[0] before its first kernel, events[1] after the schedule
+ * kernels, events[2] after the chunk kernel and events[3] after the recurrence
+ * kernel, all on the call's stream; on the segmented path events[3] follows
+ * the map pass, events[4] the scan and events[5] the recurrence (recorded only
+ * with count = 6).  The single-token step records events[0] and events[1]
+ * around its one kernel.  Events are cudaEvent_t created by the caller and
+ * must outlive the calls.  count = 0 (or events = NULL) turns the hook off;
+ * any other count returns KDA_ERR_INVALID_ARGUMENT.  Not thread-safe; intended
+ * for benchmarks.
  */
 kda_status_t kda_set_stage_events(void* const* events, int32_t count);
 
@@ -195,9 +202,13 @@ kda_status_t kda_set_stage_events(void* const* events, int32_t count);
  * kernel (one CTA per (sequence, head), state held as S^T); 3: the fused
  * launch (chunk kernel and transposed recurrence in one cooperative kernel,
  * overlapping; used only when the pairs leave at least one SM for the chunk
- * kernel, else kind 2 runs).  Process-wide,
- * applies to later calls; not thread-safe.  Any other kind returns
- * KDA_ERR_INVALID_ARGUMENT.
+ * kernel, else kind 2 runs); 4: the segmented path (each sequence's chunks
+ * split into 2..32 segments; the affine state map of every segment is found
+ * in parallel, the maps are scanned in fp32, and the value-sliced recurrence
+ * then runs all segments at once from their entering states; automatic
+ * selection takes it for few, long sequences).  Process-wide, applies to
+ * later calls, including kda_workspace_size; not thread-safe.  Any other kind
+ * returns KDA_ERR_INVALID_ARGUMENT.
  */
 kda_status_t kda_set_recurrence_kernel(int32_t kind);
 

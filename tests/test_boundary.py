@@ -94,14 +94,46 @@ def test_stage_events_validation(kda_lib):
     assert L.kda_set_stage_events(None, 0) == 0
     arr = (ctypes.c_void_p * 3)()
     assert L.kda_set_stage_events(arr, 3) == 1
+    arr6 = (ctypes.c_void_p * 6)()
+    assert L.kda_set_stage_events(arr6, 6) == 1   # null events
+    assert L.kda_set_stage_events(arr6, 5) == 1   # count neither 4 nor 6
+    assert L.kda_set_stage_events(None, 0) == 0
+
+
+def test_workspace_size_follows_segmented_selection(kda_lib):
+    """Few long sequences take the segmented path (automatically or forced): the
+    workspace adds the segment offsets and 3 fp32 128x128 tiles per (segment, head)
+    for 4..32 segments per sequence; the other kernels need none of it."""
+    L = kda_lib.lib()
+    try:
+        kda_lib.set_recurrence_kernel("sliced")
+        base = L.kda_workspace_size(1, 65536, 4, 0, 0)
+        kda_lib.set_recurrence_kernel("auto")
+        auto = L.kda_workspace_size(1, 65536, 4, 0, 0)
+        kda_lib.set_recurrence_kernel("segmented")
+        forced = L.kda_workspace_size(1, 65536, 4, 0, 0)
+        # four one-chunk sequences: no segment area under automatic selection, 2 segments forced
+        forced_short = L.kda_workspace_size(1, 64 * 4, 4, 4, 1)
+        kda_lib.set_recurrence_kernel("auto")
+        auto_short = L.kda_workspace_size(1, 64 * 4, 4, 4, 1)
+    finally:
+        kda_lib.set_recurrence_kernel("auto")
+
+    def area(P, N=1, H=4):
+        return ((N * P + 1) * 4 + 255) // 256 * 256 + N * P * H * 3 * 128 * 128 * 4
+
+    assert auto == forced
+    assert any(auto - base == area(P) for P in range(4, 33)), auto - base
+    assert auto_short < forced_short
+    assert forced_short - auto_short == area(2, N=4)
 
 
 def test_recurrence_selection_validation(kda_lib):
     L = ctypes.CDLL(kda_lib.library_path())
     L.kda_set_recurrence_kernel.argtypes = [ctypes.c_int32]
-    for kind in (-1, 4, 99):
+    for kind in (-1, 5, 99):
         assert L.kda_set_recurrence_kernel(kind) == 1  # KDA_ERR_INVALID_ARGUMENT
-    for kind in (3, 2, 1, 0):
+    for kind in (4, 3, 2, 1, 0):
         assert L.kda_set_recurrence_kernel(kind) == 0
     with pytest.raises(ValueError):
         kda_lib.set_recurrence_kernel("bogus")

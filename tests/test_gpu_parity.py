@@ -1,7 +1,8 @@
 """Parity of the CUDA path with the fp64 oracle (GPU).
 
-Every case runs once per recurrence path (value-sliced, transposed, and the
-fused launch of chunk kernel and recurrence),
+Every case runs once per recurrence path (value-sliced, transposed, the
+fused launch of chunk kernel and recurrence, and the segmented path that
+scans per-segment state maps),
 draws seeded inputs with ``gated_delta_rule_30_gb300.inputs``,
 runs ``kda.fwd`` (through the C ABI) and compares the bf16 outputs and the
 final states with the oracle over the whole tensors: relative Frobenius error
@@ -20,7 +21,7 @@ from kda_testutil import (REC_BYTES, assert_close, decode_record, errors, read_s
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True, params=["sliced", "transposed", "fused"])
+@pytest.fixture(autouse=True, params=["sliced", "transposed", "fused", "segmented"])
 def recur_kernel(request, kda_lib):
     kda_lib.set_recurrence_kernel(request.param)
     yield request.param
@@ -154,6 +155,24 @@ def test_lower_bound_range(kda_lib, oracle_mod, lb, A):
     check(oracle_mod, p, what=f"lb={lb}")
 
 
+def long_memory(p):
+    """Same inputs with exp(A_log) = 1e-4 and beta scaled by 0.05: the state keeps its
+    memory over thousands of tokens.  With the recipe's gate the decay (and the delta
+    rule's own erasure) wipe it within a few chunks, so a segment's state map M is 0
+    in fp32; here, by the oracle, dropping the first 1024 of 8192 tokens changes the
+    final state by ~10% and the later outputs by ~37%."""
+    p["A_log"] = torch.full_like(p["A_log"], float(np.log(1e-4)))
+    p["beta"] = (p["beta"].float() * 0.05).to(torch.bfloat16)
+    return p
+
+
+@pytest.mark.parametrize("T,H", [(8192, 2), (3000, 3)])
+def test_long_memory(kda_lib, oracle_mod, T, H):
+    """The state entering every chunk (every segment's map M, on the segmented path)
+    matters for the outputs and the final state."""
+    check(oracle_mod, long_memory(custom(T=T, H=H, seed=50 + H)), what=f"long memory T={T}")
+
+
 def test_one_hot_keys_overwrite(kda_lib, oracle_mod):
     """beta = 1, no decay, permuted one-hot keys (exact in bf16): a repeated key
     overwrites its slot; the query of that key reads the latest value."""
@@ -230,8 +249,8 @@ def test_fused_matches_two_kernel_path(kda_lib, recur_kernel):
 
 
 def test_automatic_path_choice(kda_lib, recur_kernel):
-    """kda_last_path reports the path automatic selection took: the fused launch
-    for few long sequences, the transposed recurrence when the pairs cover at
+    """kda_last_path reports the path automatic selection took: the segmented
+    path for very few, very long sequences, the fused launch for few long ones, the transposed recurrence when the pairs cover at
     least half the SMs, the value-sliced one in between."""
     if recur_kernel != "sliced":
         pytest.skip("run once")
@@ -239,11 +258,41 @@ def test_automatic_path_choice(kda_lib, recur_kernel):
     kda_lib.set_recurrence_kernel("auto")
     try:
         cases = [(custom(T=1024, H=2, seed=3), "fused"),                    # 2 pairs x 16 chunks
+                 (custom(T=16384, H=2, seed=3), "segmented"),              # 2 pairs x 256 chunks
                  (make("state_io", n_seqs=sms, H=1), "transposed"),        # sms pairs, short
                  (custom(lens=[100] * ((sms + 1) // 2 - 1), H=1, seed=4), "sliced")]
         for p, want in cases:
             run_gpu(p)
             assert kda_lib.last_path() == want, (p["N"] * p["H"], want, kda_lib.last_path())
+    finally:
+        kda_lib.set_recurrence_kernel(recur_kernel)
+
+
+def test_segmented_path_auto(kda_lib, oracle_mod, recur_kernel):
+    """Automatic selection takes the segmented path for 4 heads of a 16k-token
+    sequence (every case above also runs on it forced); checked against the oracle
+    with a packed batch whose sequences differ in length (segments of unequal and
+    zero length)."""
+    if recur_kernel != "sliced":
+        pytest.skip("run once")
+    kda_lib.set_recurrence_kernel("auto")
+    try:
+        # packed: automatic selection goes by the mean chunks per sequence (83 here);
+        # long memory, so each segment's map M matters
+        for p in (long_memory(custom(T=16384, H=4, seed=12)),
+                  long_memory(custom(lens=[12000, 64, 3, 9000], H=2, seed=13,
+                                     state=torch.bfloat16))):
+            check(oracle_mod, p, what="segmented auto")
+            assert kda_lib.last_path() == "segmented", kda_lib.last_path()
+            o_seg, h_seg = run_gpu(p)
+            kda_lib.set_recurrence_kernel("sliced")   # same case on one unsplit recurrence
+            check(oracle_mod, p, what="same case, sliced")
+            o_sl, h_sl = run_gpu(p)
+            kda_lib.set_recurrence_kernel("auto")
+            # different arithmetic (the final state comes from the fp32 scan), same result
+            assert not torch.equal(h_seg, h_sl)
+            assert_close(h_seg.double(), h_sl.double().numpy(), "segmented vs sliced state")
+            assert_close(o_seg.double(), o_sl.double().numpy(), "segmented vs sliced out")
     finally:
         kda_lib.set_recurrence_kernel(recur_kernel)
 
@@ -266,7 +315,8 @@ def test_malformed_cu_seqlens_reported(kda_lib):
 # ----------------------------------------------------------------------------- full sizes (sampled heads)
 
 @pytest.mark.parametrize("name,heads", [("dense_prefill", None), ("varlen_packed", [0, 13, 31]),
-                                        ("long_context", [0, 31]), ("state_io", [1, 30])])
+                                        ("long_context", [0, 31]), ("state_io", [1, 30]),
+                                        ("long_context_4h", [0, 3])])
 def test_full_size_workloads(kda_lib, oracle_mod, name, heads):
     p = make(name)
     check(oracle_mod, p, heads=heads, what=f"{name} full")
