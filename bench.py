@@ -25,6 +25,7 @@ import io
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -94,11 +95,15 @@ LAUNCHES = {"sliced": 3, "transposed": 3, "fused": 2, "decode": 1, "segmented": 
 
 
 def kernel_source_hash(kernel):
-    """Hash of a kernel's sources and the headers they include."""
+    """Hash of a kernel's sources and the headers they include, with comments and
+    whitespace removed (a comment edit does not make stored counters stale)."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel] + ("tc.cuh", "kda_internal.h"):
-        with open(os.path.join(ROOT, "gated_delta_rule_30_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "gated_delta_rule_30_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(re.sub(r"\s+", "", text).encode())
     return h.hexdigest()[:16]
 
 

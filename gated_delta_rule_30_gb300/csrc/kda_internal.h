@@ -14,6 +14,11 @@
 //      and outputs on tcgen05: kda_recur.cu (one CTA per (sequence, head,
 //      value slice), for few pairs) or kda_recur_t.cu (one CTA per (sequence,
 //      head) with the state transposed, for many pairs).
+// Other paths: kda_fused.cu runs steps 2 and 3 in one cooperative launch;
+// kda_segmented.cu splits few long sequences into segments, finds each
+// segment's state map with the recurrence kernel in map mode, scans the maps
+// and runs step 3 over the segments; kda_decode.cu handles T = 1 without
+// steps 1-3.
 #pragma once
 #include <cstddef>
 #include <cstdint>
