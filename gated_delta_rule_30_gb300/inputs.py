@@ -64,6 +64,10 @@ WORKLOADS["decode"] = Workload("decode: B=1024 T=1 H=32, fp32 state", 1024, 1, 3
 # long_context with its 32 heads split over 8 tensor-parallel GPUs: the 4 heads one GPU holds
 WORKLOADS["long_context_4h"] = Workload("long_context_4h: B=1 T=65536 H=4, fp32 state", 1, 65536,
                                         4, 6, state_dtype=torch.float32)
+# 16 heads of a 16k-token sequence (32 heads over 2 tensor-parallel GPUs): the smallest
+# split the segmented path takes automatically (4 segments of 64 chunks)
+WORKLOADS["prefill_16k_16h"] = Workload("prefill_16k_16h: B=1 T=16384 H=16, fp32 state", 1,
+                                        16384, 16, 7, state_dtype=torch.float32)
 # smaller instance of long_context used for profiler captures (inputs still exceed L2)
 WORKLOADS["long_context_8k"] = Workload("long_context_8k: B=1 T=8192 H=32, fp32 state", 1, 8192,
                                         32, 3, state_dtype=torch.float32)
