@@ -166,27 +166,34 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- oracle timing
 
 def oracle_sample(p, target_s, max_tokens=None, fixed=None):
-    """Time the fp64 oracle (as it stands) on the first S tokens of every head."""
+    """Time the fp64 oracle (as it stands) on a prefix of S tokens of every head: of the
+    packed token stream cut into whole sequences, of the first sequence when a dense
+    batch's sequences are longer than S, else of the first S // T whole sequences."""
     import torch
 
     import oracle
     oracle.build()
-    T = p["T"] if p["cu_seqlens"] is None else int(p["cu_seqlens"][-1])
+    dense = p["cu_seqlens"] is None
+    T = p["B"] * p["T"] if dense else int(p["cu_seqlens"][-1])
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     H = p["H"]
+    nseq = [1]  # sequences in the last sample
 
     def run(S):
-        # a prefix of the packed token stream, cut into whole sequences
-        if p["cu_seqlens"] is not None:
+        if not dense:
             cu = p["cu_seqlens"].tolist()
             n = max(1, max(i for i in range(len(cu)) if cu[i] <= S))
             S = cu[n]
             cu_s = torch.tensor(cu[:n + 1], dtype=torch.int32)
             h0 = None if p["initial_state"] is None else p["initial_state"][:n]
+            sl = [x[:1, :S].contiguous() for x in (p["q"], p["k"], p["v"], p["g"], p["beta"])]
         else:
             cu_s = None
-            h0 = None if p["initial_state"] is None else p["initial_state"][:1]
-        sl = [x[:1, :S].contiguous() for x in (p["q"], p["k"], p["v"], p["g"], p["beta"])]
+            n, L = (1, S) if S <= p["T"] else (min(p["B"], S // p["T"]), p["T"])
+            S = n * L
+            h0 = None if p["initial_state"] is None else p["initial_state"][:n]
+            sl = [x[:n, :L].contiguous() for x in (p["q"], p["k"], p["v"], p["g"], p["beta"])]
+        nseq[0] = n
         t0 = time.perf_counter()
         oracle.recurrent(*sl, p["scale"], p["A_log"], p["dt_bias"], p["lower_bound"],
                          initial_state=h0, cu_seqlens=cu_s, nthreads=cores)
@@ -202,12 +209,11 @@ def oracle_sample(p, target_s, max_tokens=None, fixed=None):
         if S2 > S:
             dt, ht = run(S2)
             S = S2
-    pairs = H * (1 if p["cu_seqlens"] is None else
-                 max(1, sum(1 for c in p["cu_seqlens"].tolist()[1:] if c <= S)))
-    threads = min(cores, pairs)
-    return {"value": ht / dt, "unit": UNIT, "cores": threads, "kind": "oracle", "tokens": S,
-            "sample": f"first {S} tokens x {H} heads of the workload ({ht} head-tokens), "
-                      f"fp64 C oracle, OpenMP over (sequence, head), {dt:.1f} s"}
+    threads = min(cores, H * nseq[0])
+    return {"value": ht / dt, "unit": UNIT, "cores": threads, "kind": "oracle", "tokens": ht // H,
+            "sample": f"first {ht // H} tokens ({nseq[0]} sequence(s)) x {H} heads of the "
+                      f"workload ({ht} head-tokens), fp64 C oracle, OpenMP over (sequence, "
+                      f"head), {dt:.1f} s"}
 
 
 # ----------------------------------------------------------------------------- ranks
