@@ -16,8 +16,8 @@
 //   o_v  = scale * sum_k S'[k][v] q_k
 // in fp32, and one bulk store writes the final state back.  In place (final
 // state == initial state) is safe: the store starts after every read.  The
-// bulk-copy wait is bounded; on timeout the CTA records kStatusTimeout and
-// writes nothing.
+// bulk-copy wait is bounded; on timeout the CTA records kStatusTimeout, waits
+// once more (bounded) for its copy and writes nothing.
 #include <cuda_runtime.h>
 
 #include <type_traits>
@@ -98,7 +98,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs P,
             s_fail = 1;
         }
         __syncthreads();
-        if (s_fail) return;
+        if (s_fail) {
+            if (t == 0) mbar_wait(&bar, 0);  // once more (bounded) for the copy in flight
+            return;
+        }
     }
 
     float r = 0.f;

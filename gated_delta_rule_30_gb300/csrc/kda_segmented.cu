@@ -147,8 +147,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) seg_scan_kernel(const ScanArg
         __syncthreads();  // S_{j+1} visible
     }
     if (j < P) {
-        // gave up: wait (bounded) for the copy issued in step j before leaving
-        if (t == 0 && j + 1 < P) mbar_wait(&bar[(j + 1) & 1], (uint32_t)(((j + 1) >> 1) & 1));
+        // gave up: wait once more (bounded) for the copy step j timed out on and
+        // for the one issued in step j before leaving
+        if (t == 0) {
+            mbar_wait(&bar[j & 1], (uint32_t)((j >> 1) & 1));
+            if (j + 1 < P) mbar_wait(&bar[(j + 1) & 1], (uint32_t)(((j + 1) >> 1) & 1));
+        }
         return;
     }
     if (A.hT_dtype == KDA_DTYPE_FP32) {
