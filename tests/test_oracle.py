@@ -300,6 +300,42 @@ def test_final_state_affine_in_initial_state(oracle_mod):
     assert off > 0.05 * np.abs(np.diag(M1[0])).max(), off
 
 
+@pytest.mark.parametrize("segs", [2, 3, 5])
+def test_segmented_decomposition_is_exact(oracle_mod, segs):
+    """The segmented path's algorithm, done with oracle calls: split each sequence's
+    64-token chunks into `segs` runs (run j starts at chunk floor(j * c / segs); short
+    sequences get empty runs), find every run's map (M from v = 0 and S = I, X from
+    S = 0), scan S_{j+1} = M_j S_j + X_j, rerun each run from its S_j.  Outputs and
+    final states equal one call over the whole sequences."""
+    rng = np.random.default_rng(RNG_SEED + 13)
+    lens = [200, 1, 0, 130]
+    H, K, V = 2, 8, 6
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    p = rand_problem(rng, int(cu[-1]), H, K, V, N=len(lens))
+    p["A_log"] = np.full(H, np.log(0.05))  # weak decay: runs see their entering state
+    out_ref, h_ref = run_oracle(oracle_mod, p, cu=cu)
+    acts = ("q", "k", "v", "g", "beta")
+    out = np.full_like(out_ref, np.nan)
+    for n, L in enumerate(lens):
+        c = -(-L // 64)
+        bounds = [cu[n] + min(L, 64 * ((j * c) // segs)) for j in range(segs)] + [cu[n + 1]]
+        S = p["h0"][n]                                      # [H, K, V]
+        for j in range(segs):
+            a, b = bounds[j], bounds[j + 1]
+            run = {key: (val[a:b] if key in acts else val) for key, val in p.items()}
+            run["h0"] = S[None]
+            o, _ = run_oracle(oracle_mod, run)             # outputs from the entering state
+            out[a:b] = o
+            run["h0"] = None
+            _, X = run_oracle(oracle_mod, run)
+            run["v"] = np.zeros((b - a, H, K))
+            run["h0"] = np.broadcast_to(np.eye(K), (1, H, K, K)).copy()
+            _, M = run_oracle(oracle_mod, run)
+            S = np.einsum("hik,hkv->hiv", M[0], S) + X[0]
+        np.testing.assert_allclose(S, h_ref[n], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(out, out_ref, rtol=1e-10, atol=1e-12)
+
+
 def test_packed_equals_separate(oracle_mod):
     rng = np.random.default_rng(RNG_SEED + 9)
     lens = [5, 0, 12, 1, 70]
