@@ -54,6 +54,8 @@ def lib():
     if _lib is None:
         build()
         L = ctypes.CDLL(_LIB_PATH)
+        L.kda_oracle_l2norm.restype = None
+        L.kda_oracle_l2norm.argtypes = [_dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_double]
         L.kda_oracle_log_decay.restype = ctypes.c_double
         L.kda_oracle_log_decay.argtypes = [ctypes.c_double] * 4
         L.kda_oracle_gate.restype = ctypes.c_int
@@ -146,17 +148,31 @@ def log_decay(g, A_log, dt_bias, lower_bound):
     return la.reshape(shp)
 
 
+L2NORM_EPS = 1e-6  # eps of the query/key normalisation (x / sqrt(|x|^2 + eps))
+
+
+def l2norm(x, eps=L2NORM_EPS):
+    """float64 copy of x [..., D] with every row scaled to x / sqrt(sum x^2 + eps)."""
+    a = np.array(_f64(x), dtype=np.float64, order="C", copy=True)
+    D = a.shape[-1]
+    lib().kda_oracle_l2norm(_ptr(a), int(a.size // D), D, float(eps))
+    return a
+
+
 def recurrent(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state=None,
-              cu_seqlens=None, erase=1.0, nthreads=0):
+              cu_seqlens=None, erase=1.0, nthreads=0, qk_l2norm=False):
     """Token-by-token recurrence (the definition).
 
     q, k, g: [B, T, H, K] (or [NT, H, K]); v: [..., H, V]; beta: [B, T, H];
     A_log: [H]; dt_bias: [H, K]; initial_state: [N, H, K, V] or None;
     cu_seqlens: [N + 1] or None (then N = B).  Torch bf16 activations are read
     as bf16 bit patterns and upcast exactly inside the C code; anything else is
-    converted to float64 first.  Returns (out float64 shaped like v,
+    converted to float64 first.  qk_l2norm: normalise every (token, head) row of
+    q and k first (``l2norm``, in fp64).  Returns (out float64 shaped like v,
     final_state float64 [N, H, K, V]).
     """
+    if qk_l2norm:
+        q, k = l2norm(q), l2norm(k)
     B, T = _bt(q)
     cu = _cu(cu_seqlens, B, T)
     N = len(cu) - 1

@@ -43,6 +43,12 @@
  * recurrence and expose per-chunk intermediates; it is not used to define
  * anything.
  *
+ * Optional query/key normalisation (kda_oracle_l2norm): each row x (one token
+ * of one head, K channels) becomes x / sqrt(sum_c x_c^2 + eps), applied to q
+ * and k before the recurrence.  The pages describe no normalisation inside the
+ * call (the fwd signature has no flag); this is the reading of the separate
+ * normalised entry point, with eps = 1e-6 keeping an all-zero row at zero.
+ *
  * Layouts (all row-major, contiguous):
  *   q, k, g      [NT, H, K]      NT = total tokens (B*T, or the packed length)
  *   v, out       [NT, H, V]
@@ -64,6 +70,18 @@
 #define ORACLE_ENOMEM 2
 
 int kda_oracle_abi_version(void) { return 1; }
+
+/* x[r][c] <- x[r][c] / sqrt(sum_c x[r][c]^2 + eps) for every row r of D
+ * channels (rows = tokens x heads). */
+void kda_oracle_l2norm(double* x, int64_t rows, int64_t D, double eps) {
+    for (int64_t r = 0; r < rows; ++r) {
+        double* row = x + r * D;
+        double ss = 0.0;
+        for (int64_t c = 0; c < D; ++c) ss += row[c] * row[c];
+        const double inv = 1.0 / sqrt(ss + eps);
+        for (int64_t c = 0; c < D; ++c) row[c] *= inv;
+    }
+}
 
 /* bf16 bit pattern -> exact double (bf16 is the top half of an IEEE fp32). */
 static double bf16_bits_to_double(uint16_t b) {

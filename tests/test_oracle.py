@@ -415,3 +415,75 @@ def test_workload_generator_recipe():
     assert p["initial_state"].shape == (50, 3, 128, 128)
     p2 = inputs.make(inputs.shrink(inputs.WORKLOADS["state_io"], n_seqs=50, H=3))
     assert torch.equal(p["q"], p2["q"]) and torch.equal(p["cu_seqlens"], p2["cu_seqlens"])
+
+
+# ----------------------------------------------------------------------------- q/k normalisation
+
+def test_l2norm_closed_form(oracle_mod):
+    """Each (token, head) row becomes x / sqrt(|x|^2 + eps): its norm is
+    sqrt(s / (s + eps)) with s = |x|^2, its direction is unchanged, and a zero
+    row stays zero."""
+    rng = np.random.default_rng(RNG_SEED + 700)
+    x = rng.standard_normal((7, 3, 16)) * rng.uniform(0.01, 5.0, (7, 3, 1))
+    x[2, 1] = 0.0
+    y = oracle_mod.l2norm(x)
+    s = np.sum(x * x, axis=-1)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1),
+                               np.sqrt(s / (s + oracle_mod.L2NORM_EPS)), rtol=1e-14, atol=0)
+    cos = np.sum(x * y, -1) / np.maximum(np.linalg.norm(x, axis=-1) * np.linalg.norm(y, axis=-1),
+                                         1e-300)
+    np.testing.assert_allclose(cos[s > 0], 1.0, rtol=1e-14)
+    assert np.all(y[2, 1] == 0.0)
+
+
+def _with_norm(oracle_mod, p, **kw):
+    return oracle_mod.recurrent(p["q"], p["k"], p["v"], p["g"], p["beta"], p["scale"],
+                                p["A_log"], p["dt_bias"], p["lower_bound"],
+                                initial_state=p["h0"], qk_l2norm=True, **kw)
+
+
+def test_l2norm_is_scale_free_per_row(oracle_mod):
+    """Scaling any (token, head) row of q or k by a positive factor leaves the
+    normalised pass unchanged (up to the eps term, ~1e-7 here); the same scaling
+    without normalisation changes it.  Catches normalising over the wrong axis."""
+    rng = np.random.default_rng(RNG_SEED + 701)
+    p = rand_problem(rng, 40, 3, 16, 8)
+    p["q"] = rng.standard_normal((40, 3, 16))  # |row|^2 ~ 16: eps is a 6e-8 effect
+    p["k"] = rng.standard_normal((40, 3, 16))
+    o1, h1 = _with_norm(oracle_mod, p)
+    p2 = dict(p)
+    p2["q"] = p["q"] * rng.uniform(0.5, 4.0, (40, 3, 1))
+    p2["k"] = p["k"] * rng.uniform(0.5, 4.0, (40, 3, 1))
+    o2, h2 = _with_norm(oracle_mod, p2)
+    assert np.linalg.norm(o2 - o1) <= 1e-6 * np.linalg.norm(o1)
+    assert np.linalg.norm(h2 - h1) <= 1e-6 * np.linalg.norm(h1)
+    o3, _ = run_oracle(oracle_mod, p2)
+    assert np.abs(o3 - o1).max() > 1e-2
+
+
+def test_l2norm_unit_rows_change_nothing(oracle_mod):
+    """Inputs whose rows already have unit norm: the flag changes the result only
+    through eps (relative 5e-7 on q and k)."""
+    rng = np.random.default_rng(RNG_SEED + 702)
+    p = rand_problem(rng, 50, 2, 16, 8)   # q, k unit rows
+    o0, h0 = run_oracle(oracle_mod, p)
+    o1, h1 = _with_norm(oracle_mod, p)
+    np.testing.assert_allclose(o1, o0, rtol=1e-5, atol=1e-8)
+    np.testing.assert_allclose(h1, h0, rtol=1e-5, atol=1e-8)
+    assert np.abs(o1 - o0).max() > 0  # the flag did run
+
+
+def test_l2norm_matches_brute_force(oracle_mod):
+    """Un-normalised q, k through the flag equal the numpy brute force run on rows
+    normalised in numpy."""
+    rng = np.random.default_rng(RNG_SEED + 703)
+    p = rand_problem(rng, 6, 2, 6, 4, lower_bound=-3.0)
+    p["q"] = p["q"] * rng.uniform(0.2, 3.0, (6, 2, 1))
+    p["k"] = p["k"] * rng.uniform(0.2, 3.0, (6, 2, 1))
+    out, hT = _with_norm(oracle_mod, p)
+    nq = p["q"] / np.sqrt(np.sum(p["q"] ** 2, -1, keepdims=True) + 1e-6)
+    nk = p["k"] / np.sqrt(np.sum(p["k"] ** 2, -1, keepdims=True) + 1e-6)
+    bo, bh = brute.run(nq, nk, p["v"], p["g"], p["beta"], p["scale"], p["A_log"], p["dt_bias"],
+                       p["lower_bound"], p["h0"][0])
+    np.testing.assert_allclose(out, bo, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(hT[0], bh, rtol=1e-12, atol=1e-14)

@@ -50,6 +50,10 @@ MUTATIONS = [
      "* k[l * ldk + ch];"),
     ("chunk-end decay from the first token", "gam[ch] = exp(Gl[(c - 1) * K + ch]);",
      "gam[ch] = exp(Gl[ch]);"),
+    ("l2norm without the square root", "const double inv = 1.0 / sqrt(ss + eps);",
+     "const double inv = 1.0 / (ss + eps);"),
+    ("l2norm over the first channel only", "for (int64_t c = 0; c < D; ++c) ss += row[c] * row[c];",
+     "for (int64_t c = 0; c < 1; ++c) ss += row[c] * row[c];"),
 ]
 
 PINS = [
@@ -69,6 +73,9 @@ PINS = [
     ("affine state map", pins.test_final_state_affine_in_initial_state),
     ("packed = separate", pins.test_packed_equals_separate),
     ("chunk-stage identities", pins.test_chunk_stage_identities),
+    ("l2norm closed form", pins.test_l2norm_closed_form),
+    ("l2norm scale-free rows", pins.test_l2norm_is_scale_free_per_row),
+    ("l2norm vs brute force", pins.test_l2norm_matches_brute_force),
 ]
 
 
