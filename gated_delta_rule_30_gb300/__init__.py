@@ -18,14 +18,17 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["fwd", "lib", "library_path", "workspace_size", "device_status", "KDAError",
-           "selftest_tcgen05", "set_recurrence_kernel", "set_stage_events", "last_path"]
+__all__ = ["fwd", "chunk_kda", "lib", "library_path", "workspace_size", "device_status",
+           "KDAError",
+           "selftest_tcgen05", "set_recurrence_kernel", "set_stage_events", "last_path",
+           "set_wait_limit_ns"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libkda.so")
 _lib = None
 
 KDA_OK = 0
+FWD_QK_L2NORM = 1  # kda_fwd_ex flag
 _STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED",
            3: "KDA_ERR_CUDA", 4: "KDA_ERR_TIMEOUT", 5: "KDA_ERR_DEVICE_INPUT"}
 DTYPE_NONE, DTYPE_BF16, DTYPE_FP32 = 0, 1, 2
@@ -58,6 +61,8 @@ def lib():
         L.kda_fwd.argtypes = fwd_args + [vp]
         L.kda_fwd_ws.restype = ctypes.c_int
         L.kda_fwd_ws.argtypes = fwd_args + [vp, ctypes.c_size_t, vp]
+        L.kda_fwd_ex.restype = ctypes.c_int
+        L.kda_fwd_ex.argtypes = fwd_args + [ctypes.c_uint32, vp, ctypes.c_size_t, vp]
         L.kda_workspace_size.restype = ctypes.c_size_t
         L.kda_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         L.kda_device_status.restype = ctypes.c_int
@@ -74,6 +79,8 @@ def lib():
         L.kda_set_recurrence_kernel.argtypes = [i32]
         L.kda_set_stage_events.restype = ctypes.c_int
         L.kda_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
+        L.kda_set_wait_limit_ns.restype = ctypes.c_int
+        L.kda_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         L.kda_selftest_tcgen05.restype = ctypes.c_int
         L.kda_selftest_tcgen05.argtypes = [vp, vp, vp, i32, i32, vp]
         _lib = L
@@ -106,6 +113,11 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+# Scratch buffers reused across calls, one per (device, stream).  Each buffer
+# is allocated while its stream is current, so torch's caching allocator
+# orders its reuse after that stream's work; keying by stream means calls on
+# different streams never share one (they would race on it), and replacing a
+# buffer that has grown frees memory that only its own stream has used.
 _WS_CACHE = {}
 
 
@@ -116,9 +128,11 @@ def workspace_size(B: int, T: int, H: int, num_seqs: int = 0, has_cu_seqlens: bo
     return int(n)
 
 
-def _workspace(device, nbytes):
+def _workspace(device, stream, nbytes):
+    """The cached scratch buffer of (device, stream), grown to at least nbytes.
+    Must be called with ``stream`` current on ``device``."""
     import torch
-    key = (device.type, device.index)
+    key = (device.type, device.index, stream.value)
     ws = _WS_CACHE.get(key)
     if ws is None or ws.numel() < nbytes:
         ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
@@ -127,7 +141,7 @@ def _workspace(device, nbytes):
 
 
 def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
-        final_state=None, cu_seqlens=None, workspace=None):
+        final_state=None, cu_seqlens=None, workspace=None, use_qk_l2norm_in_kernel=False):
     """KDA forward pass on the GPU; writes ``out`` (and ``final_state``) in place.
 
     q, k, g: bf16 [B, T, H, 128]; v, out: bf16 [B, T, H, 128]; beta: bf16 [B, T, H];
@@ -135,7 +149,12 @@ def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state
     [N, H, 128, 128] bf16 or fp32 (same dtype when both given) or None;
     cu_seqlens: int32 [N + 1] on the device (requires B = 1) or None.
     ``workspace``: optional uint8 device tensor of at least ``workspace_size``
-    bytes; by default a per-device buffer from torch's allocator is reused.
+    bytes; by default a buffer from torch's allocator is reused, one per (device,
+    stream), so calls on different streams may overlap.  A caller-supplied
+    workspace must not be used by another call until this call's work on the
+    current stream has finished.
+    ``use_qk_l2norm_in_kernel``: scale every (token, head) row of q and k to
+    x / sqrt(|x|^2 + 1e-6) inside the kernels first (kda_fwd_ex flag).
     Returns ``out``.
     """
     import torch
@@ -182,10 +201,34 @@ def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state
         need = L.kda_workspace_size(B, T, H, num_seqs, 1 if cu_seqlens is not None else 0)
         if need == 0:
             _check(L.kda_fwd(*args, stream))  # reports the size error
-        ws = workspace if workspace is not None else _workspace(dev, need)
-        _check(L.kda_fwd_ws(*args, ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(ws.numel()),
-                            stream))
+        ws = workspace if workspace is not None else _workspace(dev, stream, need)
+        flags = FWD_QK_L2NORM if use_qk_l2norm_in_kernel else 0
+        _check(L.kda_fwd_ex(*args, flags, ctypes.c_void_p(ws.data_ptr()),
+                            ctypes.c_size_t(ws.numel()), stream))
     return out
+
+
+def chunk_kda(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale=None, initial_state=None,
+              output_final_state=False, cu_seqlens=None, use_qk_l2norm_in_kernel=False):
+    """Allocating form of ``fwd``: returns ``(o, final_state)``.
+
+    ``o`` is a new bf16 tensor shaped like ``v``.  ``scale`` defaults to K^-0.5.
+    With ``output_final_state`` a new final state [N, H, K, V] is returned, in the
+    initial state's dtype (float32 when there is no initial state); otherwise
+    ``final_state`` is None.  Everything else is as for ``fwd``.
+    """
+    import torch
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    o = torch.empty_like(v)
+    hT = None
+    if output_final_state:
+        N = q.shape[0] if cu_seqlens is None else cu_seqlens.numel() - 1
+        dt = torch.float32 if initial_state is None else initial_state.dtype
+        hT = torch.empty((N, q.shape[2], q.shape[3], v.shape[3]), dtype=dt, device=q.device)
+    fwd(q, k, v, g, beta, scale, o, A_log, dt_bias, lower_bound, initial_state=initial_state,
+        final_state=hT, cu_seqlens=cu_seqlens, use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel)
+    return o, hT
 
 
 def fwd_alloc(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
@@ -254,6 +297,16 @@ def set_stage_events(events):
     n = len(events)
     arr = (ctypes.c_void_p * n)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(L.kda_set_stage_events(arr, n))
+
+
+def set_wait_limit_ns(limit_ns: int = 2_000_000_000, device=None):
+    """Limit of the kernels' bounded device-side waits on ``device`` (the current one
+    by default), in ns; 2e9 restores the default.  A test hook: a short limit makes
+    a wait give up, which ``device_status`` then reports as KDA_ERR_TIMEOUT."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        _check(lib().kda_set_wait_limit_ns(int(limit_ns)))
 
 
 def selftest_tcgen05(a, b, N, K):

@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdio>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -30,10 +31,13 @@ kda_status_t cuda_error(cudaError_t e, const char* where) {
 }
 void clear_error() { g_msg[0] = 0; }
 
-// ----------------------------------------------------------------------------- status word
-// One int per device: bit kStatusDeviceInput (malformed cu_seqlens seen by the
-// schedule kernel) and bit kStatusTimeout (a bounded wait gave up).
-__device__ int g_kda_status;
+// ----------------------------------------------------------------------------- status block
+// Four ints per device.  Word 0: bit kStatusDeviceInput (malformed cu_seqlens
+// seen by the schedule kernel) and bit kStatusTimeout (a bounded wait gave
+// up).  Words 2-3: the limit, in ns, of the device-side waits that can give up
+// (little-endian 64-bit; 2 s = 0x77359400), read by the kernels through
+// wait_limit_ns (tc.cuh).
+__device__ __align__(16) int g_kda_status[4] = {0, 0, 2000000000, 0};
 
 int* device_status_ptr() {
     static std::mutex mu;
@@ -282,23 +286,29 @@ kda_status_t build_problem(Problem& p, const void* q, const void* k, const void*
     p.total_tokens = total;
     // sum_n ceil(L_n / 64) <= floor((total + 63 N) / 64)
     p.max_chunks = (total + (int64_t)(kChunk - 1) * N) / kChunk;
+    p.qk_norm = false;
     return KDA_OK;
 }
 
 constexpr int kMaxStageEvents = 6;
 cudaEvent_t g_stage_events[kMaxStageEvents] = {nullptr};
 int g_stage_count = 0;  // 0: off
-int g_recur_kind = 0;   // kda_set_recurrence_kernel
+std::atomic<int> g_recur_kind{0};  // kda_set_recurrence_kernel (process-wide)
 
 void stage_mark(int i, cudaStream_t st) {
     if (i < g_stage_count) cudaEventRecord(g_stage_events[i], st);
 }
 
+// The single-token step takes a problem when the selection is automatic and it
+// applies; it reads and writes only the caller's tensors (no workspace).
+bool takes_decode(const Problem& p, int kind) { return kind == 0 && decode_applies(p); }
+
 kda_status_t run(const Problem& p, void* workspace, size_t workspace_size, cudaStream_t st) {
     if (p.N == 0) return KDA_OK;
     int* status = device_status_ptr();
     if (!status) return KDA_ERR_CUDA;
-    if (g_recur_kind == 0 && decode_applies(p)) {
+    const int sel = g_recur_kind.load();  // one reading of the selection for the whole call
+    if (takes_decode(p, sel)) {
         // one token per sequence: a single pass over the states, no chunk records
         stage_mark(0, st);
         cudaError_t e = launch_decode(p, status, st);
@@ -308,7 +318,7 @@ kda_status_t run(const Problem& p, void* workspace, size_t workspace_size, cudaS
         g_last_path = 4;
         return e == cudaSuccess ? KDA_OK : cuda_error(e, "kernel launch");
     }
-    const int segs = segment_count(p.N, p.H, p.max_chunks, g_recur_kind);
+    const int segs = segment_count(p.N, p.H, p.max_chunks, sel);
     const size_t need = workspace_bytes(p.max_chunks, p.N, p.H, segs);
     void* ws_ptr = workspace;
     bool owned = false;
@@ -349,8 +359,7 @@ kda_status_t run(const Problem& p, void* workspace, size_t workspace_size, cudaS
     // kind 3 asks for the fused launch; automatic selection takes it for few,
     // long sequences
     bool fused = false;
-    if (e == cudaSuccess && (g_recur_kind == 3 || g_recur_kind == 0) &&
-        fused_eligible(p, g_recur_kind == 3)) {
+    if (e == cudaSuccess && (sel == 3 || sel == 0) && fused_eligible(p, sel == 3)) {
         e = launch_fused(p, ws, status, st);
         if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorNotSupported) {
             cudaGetLastError();  // not resident on this device right now: run the two kernels
@@ -360,7 +369,7 @@ kda_status_t run(const Problem& p, void* workspace, size_t workspace_size, cudaS
         }
     }
     if (!fused) {
-        const int kind = recur_choose(p, g_recur_kind == 3 ? 2 : g_recur_kind);
+        const int kind = recur_choose(p, sel == 3 ? 2 : sel);
         if (e == cudaSuccess) e = launch_prep(p, ws, status, st);
         stage_mark(2, st);
         if (e == cudaSuccess) e = launch_recur(p, ws, status, st, kind);
@@ -420,6 +429,27 @@ extern "C" kda_status_t kda_fwd_ws(const void* q, const void* k, const void* v, 
     return run(p, workspace, workspace_bytes_, reinterpret_cast<cudaStream_t>(stream));
 }
 
+extern "C" kda_status_t kda_fwd_ex(const void* q, const void* k, const void* v, const void* g,
+                                   const void* beta, float scale, void* out, const float* A_log,
+                                   const float* dt_bias, float lower_bound,
+                                   const void* initial_state, kda_dtype_t initial_dtype,
+                                   void* final_state, kda_dtype_t final_dtype,
+                                   const int32_t* cu_seqlens, int32_t num_seqs, int32_t B,
+                                   int32_t T, int32_t H, int32_t K, int32_t V, uint32_t flags,
+                                   void* workspace, size_t workspace_bytes_, void* stream) {
+    clear_error();
+    if (flags & ~(uint32_t)KDA_FWD_QK_L2NORM)
+        return set_error(KDA_ERR_INVALID_ARGUMENT, "unknown flag bits");
+    Problem p;
+    kda_status_t rc = build_problem(p, q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+                                    initial_state, initial_dtype, final_state, final_dtype,
+                                    cu_seqlens, num_seqs, B, T, H, K, V);
+    if (rc != KDA_OK) return rc;
+    p.qk_norm = (flags & KDA_FWD_QK_L2NORM) != 0;
+    return run(p, workspace, workspace ? workspace_bytes_ : 0,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" size_t kda_workspace_size(int32_t B, int32_t T, int32_t H, int32_t num_seqs,
                                      int32_t has_cu_seqlens) {
     clear_error();
@@ -428,9 +458,12 @@ extern "C" size_t kda_workspace_size(int32_t B, int32_t T, int32_t H, int32_t nu
         return 0;
     }
     const int64_t N = has_cu_seqlens ? num_seqs : B;
+    const int sel = g_recur_kind.load();
+    // the single-token step uses no workspace: report the smallest valid size
+    if (sel == 0 && !has_cu_seqlens && T == 1) return 256;
     const int64_t total = (int64_t)B * T;
     const int64_t max_chunks = (total + (int64_t)(kChunk - 1) * N) / kChunk;
-    return workspace_bytes(max_chunks, N, H, segment_count(N, H, max_chunks, g_recur_kind));
+    return workspace_bytes(max_chunks, N, H, segment_count(N, H, max_chunks, sel));
 }
 
 extern "C" kda_status_t kda_device_status(void* stream) {
@@ -474,7 +507,17 @@ extern "C" kda_status_t kda_set_recurrence_kernel(int32_t kind) {
     clear_error();
     if (kind < 0 || kind > 4)
         return set_error(KDA_ERR_INVALID_ARGUMENT, "kind must be 0, 1, 2, 3 or 4");
-    g_recur_kind = kind;
+    g_recur_kind.store(kind);
+    return KDA_OK;
+}
+
+extern "C" kda_status_t kda_set_wait_limit_ns(uint64_t limit_ns) {
+    clear_error();
+    if (limit_ns == 0 || limit_ns > 2000000000ull)
+        return set_error(KDA_ERR_INVALID_ARGUMENT, "limit_ns must be in [1, 2e9]");
+    if (!device_status_ptr()) return KDA_ERR_CUDA;
+    cudaError_t e = cudaMemcpyToSymbol(g_kda_status, &limit_ns, sizeof(limit_ns), 2 * sizeof(int));
+    if (e != cudaSuccess) return cuda_error(e, "set wait limit");
     return KDA_OK;
 }
 

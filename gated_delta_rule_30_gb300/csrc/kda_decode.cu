@@ -17,7 +17,9 @@
 // in fp32, and one bulk store writes the final state back.  In place (final
 // state == initial state) is safe: the store starts after every read.  The
 // bulk-copy wait is bounded; on timeout the CTA records kStatusTimeout, waits
-// once more (bounded) for its copy and writes nothing.
+// once more for its copy (with the longer drain limit) and writes nothing.
+// With q/k normalisation (kda_fwd_ex) q and k are first scaled to
+// x / sqrt(|x|^2 + eps) by a block reduction, in fp32.
 #include <cuda_runtime.h>
 
 #include <type_traits>
@@ -40,6 +42,7 @@ struct DecodeArgs {
     const float* dt_bias;
     float lower_bound;
     float scale;
+    int qk_norm;  // normalise q and k to unit L2 norm first
     __nv_bfloat16* out;
     const void* h0;
     void* hT;
@@ -57,6 +60,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs P,
     __shared__ float sA[kDim];             // alpha_k
     __shared__ float sK[kDim];             // k_k
     __shared__ float sQ[kDim];             // q_k
+    __shared__ float sRed[2][kDecThreads / 32];  // per-warp sums of k^2, q^2 (q/k normalisation)
     __shared__ uint64_t bar;
     __shared__ int s_fail;
     constexpr uint32_t kStateBytes = kDim * kDim * sizeof(T);
@@ -64,6 +68,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs P,
     const int n = blockIdx.x / H;
     const int h = blockIdx.x - n * H;
     const int t = threadIdx.x;               // value column v, and key channel for the loads
+    const uint64_t lim = wait_limit_ns(status);  // of the state-copy wait
     const size_t row = (size_t)n * H + h;    // token row of the [N, 1, H, 128] tensors
     const size_t sbase = row * kDim * kDim;  // state [N, H, 128, 128]
 
@@ -82,8 +87,33 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs P,
         const float x = __bfloat162float(P.g[row * kDim + t]) + P.dt_bias[h * kDim + t];
         const float sp = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
         sA[t] = expf(fmaxf(-expf(P.A_log[h]) * sp, P.lower_bound));
-        sK[t] = __bfloat162float(P.k[row * kDim + t]);
-        sQ[t] = __bfloat162float(P.q[row * kDim + t]);
+        float kv = __bfloat162float(P.k[row * kDim + t]);
+        float qv = __bfloat162float(P.q[row * kDim + t]);
+        if (P.qk_norm) {
+            // x / sqrt(|x|^2 + eps) for x = k and q: block sums of the squares
+            float a = kv * kv, b = qv * qv;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                a += __shfl_xor_sync(0xffffffffu, a, o);
+                b += __shfl_xor_sync(0xffffffffu, b, o);
+            }
+            if ((t & 31) == 0) {
+                sRed[0][t >> 5] = a;
+                sRed[1][t >> 5] = b;
+            }
+            __syncthreads();
+            a = 0.f;
+            b = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecThreads / 32; ++w) {
+                a += sRed[0][w];
+                b += sRed[1][w];
+            }
+            kv *= rsqrtf(a + kL2NormEps);
+            qv *= rsqrtf(b + kL2NormEps);
+        }
+        sK[t] = kv;
+        sQ[t] = qv;
     }
     const float beta = __bfloat162float(P.beta[row]);
     const float vv = __bfloat162float(P.v[row * kDim + t]);
@@ -93,13 +123,15 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs P,
     }
     __syncthreads();  // barrier initialised (and state zeroed), gate visible
     if constexpr (!std::is_same<H0, NoState>::value) {
-        if (!mbar_wait(&bar, 0)) {
+        if (!mbar_wait(&bar, 0, lim)) {
             atomicOr(status, kStatusTimeout);
             s_fail = 1;
         }
         __syncthreads();
         if (s_fail) {
-            if (t == 0) mbar_wait(&bar, 0);  // once more (bounded) for the copy in flight
+            // gave up: wait once more, with the longer drain limit, for the copy in
+            // flight so that it never lands after the CTA has left
+            if (t == 0) mbar_drain(&bar, 0);
             return;
         }
     }
@@ -158,6 +190,7 @@ cudaError_t launch_decode(const Problem& p, int* status, cudaStream_t st) {
     a.dt_bias = p.dt_bias;
     a.lower_bound = p.lower_bound;
     a.scale = p.scale;
+    a.qk_norm = p.qk_norm ? 1 : 0;
     a.out = reinterpret_cast<__nv_bfloat16*>(p.out);
     a.h0 = p.h0;
     a.hT = p.hT;

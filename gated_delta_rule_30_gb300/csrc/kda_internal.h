@@ -96,7 +96,11 @@ struct Problem {
     int32_t B, T, H;
     int64_t total_tokens;
     int64_t max_chunks;
+    bool qk_norm;    // scale every q and k row to unit L2 norm first (kda_fwd_ex flag)
 };
+
+// eps of the q/k normalisation: x / sqrt(|x|^2 + eps)
+constexpr float kL2NormEps = 1e-6f;
 
 size_t workspace_bytes(int64_t max_chunks, int64_t N, int64_t H, int segs);
 Workspace carve_workspace(void* base, int64_t max_chunks, int64_t N, int64_t H, int segs);

@@ -10,8 +10,9 @@ using namespace prep;
 __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const __grid_constant__ PrepArgs P) {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ PrepShared S;
-    // barrier 0 over the whole 256-thread CTA is __syncthreads
-    prep_body(P, sm, S, threadIdx.x, 0u, blockIdx.x, gridDim.x, nullptr, true);
+    // barrier 0 over the whole 256-thread CTA is __syncthreads; barrier 1 spans
+    // the warps that read the key rows of the scores
+    prep_body(P, sm, S, threadIdx.x, 0u, 1u, blockIdx.x, gridDim.x, nullptr, true);
 }
 
 }  // namespace

@@ -56,11 +56,14 @@ namespace prep {
 
 constexpr int kThreads = 256;
 // shared memory map (bytes)
-constexpr uint32_t kSmQ = 0, kSmK = 16384, kSmV = 32768, kSmG = 49152;  // staging tiles [64][128]
-constexpr uint32_t kSmLeft = 0;       // 32 KB   (aliases staging once it is consumed)
-constexpr uint32_t kSmR = 32768;      // 40 KB   R_0..R_3
-constexpr uint32_t kSmVbT = 73728;    // 16 KB   (beta V)^T, K-major, M = 128 value channels, K = 64
-constexpr uint32_t kSmKbT = 90112;    // 16 KB   (beta K o E)^T
+constexpr uint32_t kSmQ = 0, kSmK = 16384, kSmG = 49152;  // staging tiles, row-major [64 t][128 c]
+// V^T as the A operand of U^T = V^T diag(beta) T^T, staged by TMA straight into the
+// MN-major core-matrix layout (8 value channels x 8 tokens per 128 B; token groups
+// 128 B apart, channel groups 1024 B apart): byte(v, t) = (v/8)*1024 + t*16 + (v%8)*2
+constexpr uint32_t kSmV = 73728;      // 16 KB   (live until the WY MMAs)
+constexpr uint32_t kSmLeft = 0;       // 32 KB   (aliases the q, k tiles once they are consumed)
+constexpr uint32_t kSmR = 32768;      // 40 KB   R_0..R_3 (aliases the g tile)
+constexpr uint32_t kSmKbT = 90112;    // 16 KB   (K o E)^T, K-major, M = 128 key channels, K = 64
 constexpr uint32_t kSmBytes = 106496;
 // after the score MMAs (alias Left / R)
 constexpr int kStr = 68;              // fp32 row stride of the 64 x 64 tiles
@@ -75,8 +78,10 @@ __host__ __device__ constexpr uint32_t d_col(int a) { return 8u * a * (a + 1); }
 constexpr uint32_t kTmemCols = 256;
 
 struct PrepArgs {
-    // TMA descriptors of q, k, v, g viewed as [tokens][H][128] bf16 with a box of
-    // 64 tokens x 1 head x 128 channels (one 16 KB row-major tile per copy)
+    // TMA descriptors of q, k, g viewed as [tokens][H][128] bf16 with a box of
+    // 64 tokens x 1 head x 128 channels (one 16 KB row-major tile per copy), and
+    // of v viewed as {8 channels, tokens, 16 channel groups, H} with a box of
+    // 8 x 64 x 16 x 1 (the MN-major operand layout of kSmV)
     CUtensorMap tm_q, tm_k, tm_v, tm_g;
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;
@@ -89,6 +94,7 @@ struct PrepArgs {
     float scale;
     int H;
     int N;
+    int qk_norm;  // normalise each q and k row (token) to unit L2 norm first
     const int32_t* flags;
     const int32_t* chunk_off;
     const ChunkInfo* info;
@@ -154,6 +160,7 @@ __device__ __forceinline__ void right_factors(const float (&al)[32], float (&rf0
 // Per-worker state that lives outside the dynamic shared-memory area.
 struct PrepShared {
     float sBeta[kChunk];
+    float sRn[2][kChunk];  // 1 / |row| of the q (0) and k (1) rows, with q/k normalisation
     float sTot[2][kDim];  // product of each half's alphas
     float sQf[2][kDim];   // prod_{s=32}^{39} and prod_{s=32}^{55} alpha_s
     uint64_t bar;       // MMA completion
@@ -167,14 +174,22 @@ struct PrepShared {
 __device__ __forceinline__ void sub_sync(uint32_t bar_id) {
     asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kThreads) : "memory");
 }
-// One TMA tile copy (box of the tensor map at coordinates {x, y, z}) into shared
-// memory, completing on `bar`.
+// One TMA tile copy (box of the tensor map at coordinates {x, y, z} / {x, y, z, w})
+// into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
                                             uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
         "%3, %4}], [%5];" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            int w, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar))
         : "memory");
 }
 __device__ __forceinline__ void st_release_gpu(int* p, int v) {
@@ -230,13 +245,15 @@ __device__ __forceinline__ void level_products(const float* sAT, float* sT, floa
 
 // One chunk-kernel worker: `kThreads` threads (thread index `tid`), the
 // shared-memory area `sm` (kSmBytes, 1024-byte aligned) and the small state
-// `S`, synchronised by named barrier `bar_id`.  It processes the (chunk, head)
+// `S`, synchronised by named barrier `bar_id` (and `bar_k`, over the half of
+// the worker's warps that read the key rows of the scores).  It processes the (chunk, head)
 // items first_item, first_item + item_stride, ...; with `ready` non-null it
 // publishes ready[item] = 1 (release, GPU scope) once an item's record is
 // complete.
 __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepShared& S,
                                           const int tid, const uint32_t bar_id,
-                                          const int first_item, const int item_stride, int* ready,
+                                          const uint32_t bar_k, const int first_item,
+                                          const int item_stride, int* ready,
                                           const bool relinquish) {
 
     if (P.flags[0] != 1) return;
@@ -245,6 +262,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     if (tid == 0) S.s_abort = (*((volatile int*)P.status) & kStatusTimeout) ? 1 : 0;
     sub_sync(bar_id);
     if (S.s_abort) return;
+    const uint64_t lim = wait_limit_ns(P.status);  // of every wait that may give up
     const int H = P.H;
     const int n_items = P.chunk_off[P.N] * H;  // valid (chunk, head) pairs
     int item = first_item;
@@ -265,7 +283,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
             mbar_arrive_expect_tx(&S.bar_qkv, 3 * kChunk * kDim * 2);
             tma_load_3d(sm + kSmQ, &P.tm_q, 0, hh, c.tok0, &S.bar_qkv);
             tma_load_3d(sm + kSmK, &P.tm_k, 0, hh, c.tok0, &S.bar_qkv);
-            tma_load_3d(sm + kSmV, &P.tm_v, 0, hh, c.tok0, &S.bar_qkv);
+            tma_load_4d(sm + kSmV, &P.tm_v, 0, c.tok0, 0, hh, &S.bar_qkv);
         }
         if (tid < kChunk) S.sBeta[tid] = beta_t;
     };
@@ -296,6 +314,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     const uint32_t tbase = S.tmem_base;
     uint32_t tph = 0;       // phase of bar_g / bar_qkv for the current item
     bool pending = true;    // an issued staging not yet waited for
+    int drain_mma = -1;     // after giving up on an MMA wait: the S.bar phase still owed
 
     for (;;) {
     const int len = ci.len;
@@ -304,7 +323,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     const bool has_next = next < n_items;
     const int chunk_n = has_next ? next / H : chunk;
     const int h_n = has_next ? next - chunk_n * H : h;
-    if (!mbar_wait(&S.bar_g, tph)) {
+    if (!mbar_wait(&S.bar_g, tph, lim)) {
         atomicOr(P.status, kStatusTimeout);
         S.s_abort = 1;
     }
@@ -334,36 +353,73 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         }
         S.sTot[half][ch] = prod;
     }
-    if (!mbar_wait(&S.bar_qkv, tph)) {
+    if (mbar_wait(&S.bar_qkv, tph, lim)) {
+        pending = false;
+    } else {
         atomicOr(P.status, kStatusTimeout);
         S.s_abort = 1;
     }
-    pending = false;
-    if (len < kChunk) {
+    if (len < kChunk && !pending) {
         // zero the rows of tokens past the chunk's end in the q, k, v tiles
         for (int e = tid; e < 3 * kChunk * 16; e += kThreads) {
             const int tile = e / (kChunk * 16), r = (e / 16) % kChunk, piece = e & 15;
-            if (r >= len)
-                *reinterpret_cast<uint4*>(sm + tile * 16384 + r * 256 + piece * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
+            if (r >= len) {
+                uint8_t* p = tile < 2 ? sm + tile * 16384 + r * 256 + piece * 16
+                                      : sm + kSmV + piece * 1024 + r * 16;  // channel group `piece`
+                *reinterpret_cast<uint4*>(p) = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
     }
     sub_sync(bar_id);           // q, k, v, S.sTot, S.sQf visible
     if (S.s_abort) break;
     uint32_t qp[16], kp[16];
+    if (P.qk_norm) {
+        // 1 / sqrt(|x|^2 + eps) of each q row (r < 64) and k row (r >= 64), two
+        // threads per row; zeroed padding rows stay zero
+        {
+            const int r = tid >> 1, hf = tid & 1;
+            const uint4* rowp = reinterpret_cast<const uint4*>(
+                sm + (r < kChunk ? kSmQ : kSmK) + (r & (kChunk - 1)) * 256 + hf * 128);
+            float ss = 0.f;
 #pragma unroll
-    for (int u = 0; u < 32; u += 2) {
-        const int t = t0 + u;
-        qp[u / 2] = pack_bf16(lds_bf16(sm, kSmQ + t * 256 + ch * 2),
-                              lds_bf16(sm, kSmQ + (t + 1) * 256 + ch * 2));
-        kp[u / 2] = pack_bf16(lds_bf16(sm, kSmK + t * 256 + ch * 2),
-                              lds_bf16(sm, kSmK + (t + 1) * 256 + ch * 2));
+            for (int w = 0; w < 8; ++w) {
+                const uint4 x = rowp[w];
+                const uint32_t e[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    ss = fmaf(bf16_lo(e[j]), bf16_lo(e[j]), ss);
+                    ss = fmaf(bf16_hi(e[j]), bf16_hi(e[j]), ss);
+                }
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            if (hf == 0) S.sRn[r / kChunk][r & (kChunk - 1)] = rsqrtf(ss + kL2NormEps);
+        }
+        sub_sync(bar_id);
+        // the normalised rows, rounded to bf16 like the inputs
+#pragma unroll
+        for (int u = 0; u < 32; u += 2) {
+            const int t = t0 + u;
+            qp[u / 2] = pack_bf16(lds_bf16(sm, kSmQ + t * 256 + ch * 2) * S.sRn[0][t],
+                                  lds_bf16(sm, kSmQ + (t + 1) * 256 + ch * 2) * S.sRn[0][t + 1]);
+            kp[u / 2] = pack_bf16(lds_bf16(sm, kSmK + t * 256 + ch * 2) * S.sRn[1][t],
+                                  lds_bf16(sm, kSmK + (t + 1) * 256 + ch * 2) * S.sRn[1][t + 1]);
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < 32; u += 2) {
+            const int t = t0 + u;
+            qp[u / 2] = pack_bf16(lds_bf16(sm, kSmQ + t * 256 + ch * 2),
+                                  lds_bf16(sm, kSmQ + (t + 1) * 256 + ch * 2));
+            kp[u / 2] = pack_bf16(lds_bf16(sm, kSmK + t * 256 + ch * 2),
+                                  lds_bf16(sm, kSmK + (t + 1) * 256 + ch * 2));
+        }
     }
 #define KV(u) ((u) & 1 ? bf16_hi(kp[(u) / 2]) : bf16_lo(kp[(u) / 2]))
 #define QV(u) ((u) & 1 ? bf16_hi(qp[(u) / 2]) : bf16_lo(qp[(u) / 2]))
     const float P0 = S.sTot[0][ch], P1 = S.sTot[1][ch];
     {
-        // prefix pass: (beta K o E)^T to smem, scale * (Q o E) to the record
+        // prefix pass: (K o E)^T to smem, scale * (Q o E) to the record (beta
+        // enters the WY products through the shared operand diag(beta) T^T)
         float E = half ? P0 : 1.f;
 #pragma unroll
         for (int tg = 0; tg < 4; ++tg) {
@@ -372,7 +428,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
             for (int u = 0; u < 8; ++u) {
                 const int uu = tg * 8 + u;
                 E *= al[uu];
-                kb[u] = S.sBeta[t0 + uu] * KV(uu) * E;
+                kb[u] = KV(uu) * E;
                 qh[u] = P.scale * QV(uu) * E;
             }
             sts_v4f(smem_addr(sm + kSmKbT + kmaj_off(ch, t0 + tg * 8, 128, 1024)), kb);
@@ -391,17 +447,6 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
                 F *= al[uu];
             }
             stg_v4f(rec + kRecKT + kmaj_off(ch, t0 + tg * 8, 128, 1024), kt);
-        }
-        // (beta V)^T (thread = value channel)
-#pragma unroll
-        for (int tg = 0; tg < 4; ++tg) {
-            float vb[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int t = t0 + tg * 8 + u;
-                vb[u] = S.sBeta[t] * lds_bf16(sm, kSmV + t * 256 + ch * 2);
-            }
-            sts_v4f(smem_addr(sm + kSmVbT + kmaj_off(ch, t0 + tg * 8, 128, 1024)), vb);
         }
     }
     sub_sync(bar_id);  // staging fully consumed; Left / R may now overwrite it
@@ -510,13 +555,16 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
             mma_bf16(tbase, dl + 16u * kk, dr + 16u * kk, idesc, kk > 0 ? 1u : 0u);
         mma_commit(&S.bar);
     }
-    if (!mbar_wait(&S.bar, 0)) {
+    if (!mbar_wait(&S.bar, 0, lim)) {
         atomicOr(P.status, kStatusTimeout);
         S.s_abort = 1;
     }
     tc_fence_after();
     sub_sync(bar_id);
-    if (S.s_abort) break;
+    if (S.s_abort) {
+        drain_mma = 0;
+        break;
+    }
 
     // ---------------------------------------------------------------- score read-out
     // TMEM lane quarter w % 4 holds k rows (quarters 0, 1) or q rows (2, 3) of
@@ -566,22 +614,53 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
                 }
             }
         }
-        if (qd == 2) {
-            // tokens 0..31 attend to no key in 32..63: zero those record columns
-#pragma unroll
-            for (int jg = 0; jg < 2; ++jg) {
-                const int j0 = 32 + 16 * hj + 8 * jg;
-                stg_v4(rec + kRecAQ + kmaj_off(i, j0, 128, 1024), 0u, 0u, 0u, 0u);
-                stg_v4(rec + kRecAQL + kmaj_off(i, j0, 128, 1024), 0u, 0u, 0u, 0u);
-            }
-        }
-        // zero the strictly upper 16 x 16 blocks of T
         float* sT = reinterpret_cast<float*>(sm + kSmT);
-        for (int e = tid; e < 6 * 256; e += kThreads) {
-            const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-            const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            sT[(16 * a + r) * kStr + 16 * b + c] = 0.f;
+        if (!is_k) {
+            if (qd == 2) {
+                // tokens 0..31 attend to no key in 32..63: zero those record columns
+#pragma unroll
+                for (int jg = 0; jg < 2; ++jg) {
+                    const int j0 = 32 + 16 * hj + 8 * jg;
+                    stg_v4(rec + kRecAQ + kmaj_off(i, j0, 128, 1024), 0u, 0u, 0u, 0u);
+                    stg_v4(rec + kRecAQL + kmaj_off(i, j0, 128, 1024), 0u, 0u, 0u, 0u);
+                }
+            }
+            // zero the strictly upper 16 x 16 blocks of T (q-row warps, while the
+            // k-row warps invert the diagonal blocks)
+            const int qt = 64 * hj + 32 * (qd - 2) + lane;  // 0..127
+            for (int e = qt; e < 6 * 256; e += 128) {
+                const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                sT[(16 * a + r) * kStr + 16 * b + c] = 0.f;
+            }
+        } else {
+            // A^T is complete once the four k-row warps have stored it; warps 0 and 1
+            // then invert the four 16 x 16 diagonal blocks of I + A by forward
+            // substitution (lanes 0-15 one block, 16-31 the next; lane = column j),
+            // overlapping the q-row warps' record stores
+            asm volatile("bar.sync %0, %1;" ::"r"(bar_k), "n"(kThreads / 2) : "memory");
+            if (warp < 2) {
+                const int o = 16 * (2 * warp + (lane >> 4)), j = lane & 15;
+                const float* sA = sAT;  // sA[l][i] = A[i][l]
+                float tc[16];
+#pragma unroll
+                for (int l = 0; l < 16; ++l) tc[l] = (l == j) ? 1.f : 0.f;
+#pragma unroll
+                for (int ii = 1; ii < 16; ++ii) {
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int l = 0; l < ii; ++l) {
+                        if (l & 1)
+                            s1 = fmaf(sA[(o + l) * kStr + o + ii], tc[l], s1);
+                        else
+                            s0 = fmaf(sA[(o + l) * kStr + o + ii], tc[l], s0);
+                    }
+                    if (ii > j) tc[ii] = -(s0 + s1);
+                }
+#pragma unroll
+                for (int ii = 0; ii < 16; ++ii) sT[(o + ii) * kStr + o + j] = tc[ii];
+            }
         }
     }
     tc_fence_before();
@@ -598,40 +677,21 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         const float* sAT = reinterpret_cast<const float*>(sm + kSmA);  // sAT[l][i] = A[i][l]
         float* sT = reinterpret_cast<float*>(sm + kSmT);
         float* sX = reinterpret_cast<float*>(sm + kSmX);
-        if (warp < 4 && lane < 16) {
-            // diagonal block `warp`, column `lane`, by forward substitution
-            const int o = 16 * warp, j = lane;
-            float tc[16];
-#pragma unroll
-            for (int l = 0; l < 16; ++l) tc[l] = (l == j) ? 1.f : 0.f;
-#pragma unroll
-            for (int i = 1; i < 16; ++i) {
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                for (int l = 0; l < i; ++l) {
-                    if (l & 1)
-                        s1 = fmaf(sAT[(o + l) * kStr + o + i], tc[l], s1);
-                    else
-                        s0 = fmaf(sAT[(o + l) * kStr + o + i], tc[l], s0);
-                }
-                if (i > j) tc[i] = -(s0 + s1);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) sT[(o + i) * kStr + o + j] = tc[i];
-        }
-        sub_sync(bar_id);
+        // (diagonal blocks: inverted above, after the score read-out)
         // off-diagonal blocks, one diagonal distance d at a time
         level_products<1>(sAT, sT, sX, tid, bar_id);
         level_products<2>(sAT, sT, sX, tid, bar_id);
         level_products<3>(sAT, sT, sX, tid, bar_id);
-        // T^T as MN-major B operand: element (n = t, k = s), k-groups 128 B, n-groups 1024 B
+        // diag(beta) T^T as MN-major B operand: element (n = t, k = s) = beta_s T[t][s],
+        // k-groups 128 B, n-groups 1024 B
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
             const int e = tid + kThreads * it;   // 512 vectors: (t-group, s)
             const int s = e & 63, tg = e >> 6;
+            const float bs = S.sBeta[s];
             float x[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) x[u] = sT[(tg * 8 + u) * kStr + s];
+            for (int u = 0; u < 8; ++u) x[u] = sT[(tg * 8 + u) * kStr + s] * bs;
             sts_v4f(smem_addr(sm + kSmTT + mnmaj_off(tg * 8, s, 128, 1024)), x);
         }
     }
@@ -642,27 +702,31 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     // ---------------------------------------------------------------- W^T, U^T MMAs
     if (tid == 0) {
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16_f32(128, 64, false, true);
+        const uint32_t idesc_w = idesc_bf16_f32(128, 64, false, true);  // A K-major
+        const uint32_t idesc_u = idesc_bf16_f32(128, 64, true, true);   // A MN-major (V tile)
         const uint32_t bT = smem_addr(sm + kSmTT);
         const uint32_t aK = smem_addr(sm + kSmKbT);
-        const uint32_t aV = smem_addr(sm + kSmVbT);
+        const uint32_t aV = smem_addr(sm + kSmV);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
             mma_bf16(tbase + 0, smem_desc(aK + kk * 256, 128, 1024),
-                     smem_desc(bT + kk * 256, 128, 1024), idesc, kk > 0 ? 1u : 0u);
+                     smem_desc(bT + kk * 256, 128, 1024), idesc_w, kk > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
             mma_bf16(tbase + 64, smem_desc(aV + kk * 256, 128, 1024),
-                     smem_desc(bT + kk * 256, 128, 1024), idesc, kk > 0 ? 1u : 0u);
+                     smem_desc(bT + kk * 256, 128, 1024), idesc_u, kk > 0 ? 1u : 0u);
         mma_commit(&S.bar);
     }
-    if (!mbar_wait(&S.bar, 1)) {
+    if (!mbar_wait(&S.bar, 1, lim)) {
         atomicOr(P.status, kStatusTimeout);
         S.s_abort = 1;
     }
     tc_fence_after();
     sub_sync(bar_id);
-    if (S.s_abort) break;
+    if (S.s_abort) {
+        drain_mma = 1;
+        break;
+    }
 
     // the staging area is free again: start the next item's copies
     float beta_n = 0.f;
@@ -677,15 +741,19 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     {
         const bool is_w = warp < 4;
         const uint32_t col0 = is_w ? 0u : 64u;
+        uint32_t r[4][16];  // all four loads in flight before one wait
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld16(taddr(tbase, 32u * (warp & 3), col0 + 16u * c), r[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_fence16(r[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            uint32_t r[16];
-            tmem_load16(taddr(tbase, 32u * (warp & 3), col0 + 16u * c), r);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 float x[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) x[u] = __uint_as_float(r[8 * hh + u]);
+                for (int u = 0; u < 8; ++u) x[u] = __uint_as_float(r[c][8 * hh + u]);
                 if (is_w)
                     stg_v4f(rec + kRecWQ + mnmaj_off(16 * c + 8 * hh, ch, 128, 2048), x);
                 else
@@ -710,11 +778,13 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     tc_fence_before();
     }  // item loop
 
-    if (pending) {
+    if (pending && tid == 0) {
         // an aborted worker waits (bounded) for its own tile copies before leaving
-        mbar_wait(&S.bar_g, tph);
-        mbar_wait(&S.bar_qkv, tph);
+        mbar_drain(&S.bar_g, tph);
+        mbar_drain(&S.bar_qkv, tph);
     }
+    // ... and for an MMA it stopped waiting for, before its TMEM is freed
+    if (drain_mma >= 0 && tid == 0) mbar_drain(&S.bar, (uint32_t)drain_mma);
     tc_fence_before();
     sub_sync(bar_id);
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
@@ -751,6 +821,22 @@ inline bool encode_tile_map(CUtensorMap* m, const void* base, int64_t tokens, in
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [tokens][H][128] bf16 viewed as {8 channels, tokens, 16 channel groups, H}
+// -> boxes of 8 x 64 x 16 x 1 that land as [group][token][8 channels], the
+// MN-major core-matrix layout of a 128-channel x 64-token operand (channel
+// groups 1024 B apart, token groups 128 B apart).
+inline bool encode_operand_map(CUtensorMap* m, const void* base, int64_t tokens, int H) {
+    const EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {8u, (cuuint64_t)tokens, (cuuint64_t)(kDim / 8), (cuuint64_t)H};
+    const cuuint64_t strides[3] = {(cuuint64_t)H * kDim * 2, 16u, (cuuint64_t)kDim * 2};  // bytes
+    const cuuint32_t box[4] = {8u, (cuuint32_t)kChunk, (cuuint32_t)(kDim / 8), 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Arguments of the chunk kernel; false if a tensor map cannot be built.
 inline bool make_prep_args(const Problem& p, const Workspace& ws, int* status, PrepArgs& a) {
     a.q = reinterpret_cast<const __nv_bfloat16*>(p.q);
@@ -764,6 +850,7 @@ inline bool make_prep_args(const Problem& p, const Workspace& ws, int* status, P
     a.scale = p.scale;
     a.H = p.H;
     a.N = p.N;
+    a.qk_norm = p.qk_norm ? 1 : 0;
     a.flags = ws.flags;
     a.chunk_off = ws.chunk_off;
     a.info = ws.info;
@@ -771,7 +858,7 @@ inline bool make_prep_args(const Problem& p, const Workspace& ws, int* status, P
     a.status = status;
     return encode_tile_map(&a.tm_q, p.q, p.total_tokens, p.H) &&
            encode_tile_map(&a.tm_k, p.k, p.total_tokens, p.H) &&
-           encode_tile_map(&a.tm_v, p.v, p.total_tokens, p.H) &&
+           encode_operand_map(&a.tm_v, p.v, p.total_tokens, p.H) &&
            encode_tile_map(&a.tm_g, p.g, p.total_tokens, p.H);
 }
 

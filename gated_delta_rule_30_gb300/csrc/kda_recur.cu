@@ -132,12 +132,14 @@ struct StateIO<__nv_bfloat16> {
 };
 struct NoState {};
 
-// Bounded wait that records a timeout and raises the CTA's abort flag.
-#define WAIT_OR_ABORT(bar, parity)                         \
-    if (!mbar_wait((bar), (parity))) {                     \
-        atomicOr(P.status, kStatusTimeout);                \
-        s_abort = 1;                                       \
-        break;                                             \
+// Bounded wait that records a timeout and raises the CTA's abort flag.  When a
+// whole warp waits, its lanes see the same barrier state and time in the same
+// instructions, so they leave the loop together.
+#define WAIT_OR_ABORT(bar, parity)                  \
+    if (!mbar_wait((bar), (parity), lim)) {         \
+        atomicOr(P.status, kStatusTimeout);         \
+        s_abort = 1;                             \
+        break;                                      \
     }
 
 // H0 / HT: float, __nv_bfloat16 or NoState; kMap: map mode (H0 = NoState, HT = float)
@@ -149,9 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
     extern __shared__ __align__(1024) uint8_t sm[];
     // full/empty: record ring; s_ready: snapshot written; mma1: X = [W;Q].S done;
     // d_ready: Delta written; mma2s: state update done; mma2o[b]: output update
-    // of the chunk in X[b] done; x_free[b]: the output warps have read X[b]
+    // of the chunk in X[b] done; x_free[b]: the output warps have read X[b];
+    // mma_done: every MMA the CTA issued has completed (before TMEM is freed)
     constexpr int NS = L::kStages;
-    __shared__ uint64_t full[NS], empty[NS], s_ready, mma1, d_ready, mma2s, mma2o[2], x_free[2];
+    __shared__ uint64_t full[NS], empty[NS], s_ready, mma1, d_ready, mma2s, mma2o[2], x_free[2],
+        mma_done;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
@@ -161,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
     if (threadIdx.x == 0) s_abort = (*((volatile int*)P.status) & kStatusTimeout) ? 1 : 0;
     __syncthreads();
     if (s_abort) return;
+    const uint64_t lim = wait_limit_ns(P.status);  // of every wait that may give up
     const int H = P.H;
     const int gslice = blockIdx.x % kGridSlices;
     const bool lin = kMap && gslice >= kSlices;  // map mode: this CTA evolves the identity
@@ -191,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
             mbar_init(&mma2o[b], 1);
             mbar_init(&x_free[b], 64);
         }
+        mbar_init(&mma_done, 1);
         mbar_fence_init();
         s_abort = 0;
     }
@@ -252,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
             }
             // drain: every issued fill must have landed before the CTA exits
             for (int s = 0; s < NS; ++s)
-                if (fills[s] > 0 && !mbar_wait(&full[s], (uint32_t)((fills[s] - 1) & 1)))
+                if (fills[s] > 0 && !mbar_drain(&full[s], (uint32_t)((fills[s] - 1) & 1)))
                     atomicOr(P.status, kStatusTimeout);
         }
     } else if (warp == 5) {
@@ -326,6 +332,12 @@ __global__ void __launch_bounds__(kThreads, 1) recur_kernel(const RecurArgs P) {
             __syncwarp();
             if (!kMap) issue_out(i);
         }
+        // every MMA issued above has completed before TMEM is freed (after a
+        // normal end the consumers already waited for them; after giving up
+        // some may still be running)
+        if (elect_one()) mma_commit(&mma_done);
+        __syncwarp();
+        if (!mbar_drain(&mma_done, 0)) atomicOr(P.status, kStatusTimeout);
     } else if (warp < 4) {
         // ------------------------------------------------------------ state / epilogue warps
         const int row = tid;  // TMEM lane: key channel for S, token row for X

@@ -125,8 +125,8 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
-// Wait (bounded, 2 s) until *flag is non-zero.
-__device__ __forceinline__ bool wait_flag(const int* flag) {
+// Wait (bounded by `limit` ns) until *flag is non-zero.
+__device__ __forceinline__ bool wait_flag(const int* flag, uint64_t limit) {
     if (ld_acquire_gpu(flag) != 0) return true;
     const uint64_t t0 = global_ns();
     while (true) {
@@ -134,18 +134,20 @@ __device__ __forceinline__ bool wait_flag(const int* flag) {
             __nanosleep(64);
             if (ld_acquire_gpu(flag) != 0) return true;
         }
-        if (global_ns() - t0 > 2000000000ull) return false;
+        if (global_ns() - t0 > limit) return false;
     }
 }
 
 // Small per-block state that lives outside the dynamic shared-memory area.
-// full/empty: record ring; s_ready: snapshot written; mma1: X^T ready;
+// full/empty: record ring; s_ready[r]: round r of the snapshot written (key
+// channels 64 h + 32 r .. + 31 of both halves h); mma1: X^T ready;
 // d_ready: Delta^T written; mma2s: state updated; mma2o[b]: outputs of the
 // chunk in X[b] complete; x_free[b]: the output warps have read X[b];
-// tile_full[b]: output tile b is written
+// tile_full[b]: output tile b is written; mma_done: every MMA the block
+// issued has completed (waited for once, before TMEM is freed)
 struct RecurTShared {
-    uint64_t full[kStages], empty[kStages], s_ready, mma1, d_ready, mma2s, mma2o[2], x_free[2],
-        tile_full[2];
+    uint64_t full[kStages], empty[kStages], s_ready[2], mma1, d_ready, mma2s, mma2o[2], x_free[2],
+        tile_full[2], mma_done;
     uint32_t tmem_base;
     int s_abort;
 };
@@ -158,12 +160,14 @@ __device__ __forceinline__ void tmem_st8(uint32_t ta, const uint32_t (&r)[8]) {
         : "memory");
 }
 
-// Bounded wait that records a timeout and raises the CTA's abort flag.
-#define WAIT_OR_ABORT(bar, parity)              \
-    if (!mbar_wait((bar), (parity))) {          \
-        atomicOr(P.status, kStatusTimeout);     \
-        S.s_abort = 1;                          \
-        break;                                  \
+// Bounded wait that records a timeout and raises the CTA's abort flag.  When a
+// whole warp waits, its lanes see the same barrier state and time in the same
+// instructions, so they leave the loop together.
+#define WAIT_OR_ABORT(bar, parity)                  \
+    if (!mbar_wait((bar), (parity), lim)) {         \
+        atomicOr(P.status, kStatusTimeout);         \
+        S.s_abort = 1;                             \
+        break;                                      \
     }
 
 // The recurrence of (sequence, head) pair `pair` on kThreads threads (thread
@@ -180,6 +184,7 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
     if (tid == 0) S.s_abort = (*((volatile int*)P.status) & kStatusTimeout) ? 1 : 0;
     all_sync(bar_all);
     if (S.s_abort) return;
+    const uint64_t lim = wait_limit_ns(P.status);  // of every wait that may give up
     const int H = P.H;
     const int h = pair % H;
     const int n = pair / H;
@@ -211,7 +216,8 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], 1);
         }
-        mbar_init(&S.s_ready, 32 * kEpiWarps);
+        mbar_init(&S.s_ready[0], 32 * kEpiWarps);
+        mbar_init(&S.s_ready[1], 32 * kEpiWarps);
         mbar_init(&S.mma1, 1);
         mbar_init(&S.d_ready, 32 * kEpiWarps);
         mbar_init(&S.mma2s, 1);
@@ -220,6 +226,7 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
             mbar_init(&S.x_free[b], 32 * kOutWarps);
             mbar_init(&S.tile_full[b], 32 * kOutWarps);
         }
+        mbar_init(&S.mma_done, 1);
         mbar_fence_init();
         S.s_abort = 0;
     }
@@ -249,44 +256,45 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
             const uint32_t ph = (uint32_t)(i & 1);
             const uint8_t* st = sm + s * kStageBytes;
             WAIT_OR_ABORT(&S.full[s], (uint32_t)((i / kStages) & 1));
-            // snapshot: bf16 S^T for MMA1, and S^T <- S^T Diag(gamma) for MMA2s
+            // snapshot in two rounds of 32 key channels: the bf16 S^T columns
+            // MMA1 reads are written and signalled first (MMA1 starts on round 0's
+            // K-steps while round 1 is converted); the chunk decay
+            // S^T <- S^T Diag(gamma), which only MMA2s needs, follows off that path
+            // (the wait::st before d_ready covers its stores)
             {
                 const float4* gam4 =
                     reinterpret_cast<const float4*>(st + kRecGam) + 16 * hc;  // 64 channels
 #pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 32) {
-                    uint32_t r[2][16];
-                    tmem_ld16(lane_base + kColS + 64 * hc + c0, r[0]);
-                    tmem_ld16(lane_base + kColS + 64 * hc + c0 + 16, r[1]);
-                    float gam[32];
-#pragma unroll
-                    for (int w = 0; w < 8; ++w) {
-                        const float4 g4 = gam4[c0 / 4 + w];
-                        gam[4 * w] = g4.x;
-                        gam[4 * w + 1] = g4.y;
-                        gam[4 * w + 2] = g4.z;
-                        gam[4 * w + 3] = g4.w;
-                    }
+                for (int r = 0; r < 2; ++r) {
+                    const uint32_t c0 = 64 * hc + 32 * r;  // first key channel of the round
+                    uint32_t x[2][16];
+                    tmem_ld16(lane_base + kColS + c0, x[0]);
+                    tmem_ld16(lane_base + kColS + c0 + 16, x[1]);
                     tmem_wait_ld();
-                    reg_fence16(r[0]);
-                    reg_fence16(r[1]);
+                    reg_fence16(x[0]);
+                    reg_fence16(x[1]);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u)
+                        pk[u] = pack_bf16(__uint_as_float(x[u >> 3][(2 * u) & 15]),
+                                          __uint_as_float(x[u >> 3][(2 * u + 1) & 15]));
+                    tmem_st16(lane_base + kColSb + c0 / 2, pk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&S.s_ready[r]);
 #pragma unroll
                     for (int g = 0; g < 2; ++g) {
-                        uint32_t pk[8];
 #pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            pk[u] = pack_bf16(__uint_as_float(r[g][2 * u]),
-                                              __uint_as_float(r[g][2 * u + 1]));
-                        tmem_st8(lane_base + kColSb + 32 * hc + (c0 + 16 * g) / 2, pk);
-#pragma unroll
-                        for (int u = 0; u < 16; ++u)
-                            r[g][u] = __float_as_uint(__uint_as_float(r[g][u]) * gam[16 * g + u]);
-                        tmem_st16(lane_base + kColS + 64 * hc + c0 + 16 * g, r[g]);
+                        for (int w = 0; w < 4; ++w) {
+                            const float4 g4 = gam4[8 * r + 4 * g + w];
+                            x[g][4 * w + 0] = __float_as_uint(__uint_as_float(x[g][4 * w + 0]) * g4.x);
+                            x[g][4 * w + 1] = __float_as_uint(__uint_as_float(x[g][4 * w + 1]) * g4.y);
+                            x[g][4 * w + 2] = __float_as_uint(__uint_as_float(x[g][4 * w + 2]) * g4.z);
+                            x[g][4 * w + 3] = __float_as_uint(__uint_as_float(x[g][4 * w + 3]) * g4.w);
+                        }
+                        tmem_st16(lane_base + kColS + c0 + 16 * g, x[g]);
                     }
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&S.s_ready);
             }
             // Delta^T[v][t] = U[t][v] - X_W[v][t] for this thread's 32 tokens
             uint32_t uw[16];
@@ -370,7 +378,7 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
                             kRecBytes);
                     if (ready) {
                         // the record is written by a chunk-kernel worker of the same launch
-                        if (!wait_flag(ready + (size_t)(c_begin + i) * H + h)) {
+                        if (!wait_flag(ready + (size_t)(c_begin + i) * H + h, lim)) {
                             atomicOr(P.status, kStatusTimeout);
                             S.s_abort = 1;
                             break;
@@ -385,7 +393,7 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
                 }
                 // drain: every issued fill must have landed before the CTA exits
                 for (int s = 0; s < kStages; ++s)
-                    if (fills[s] > 0 && !mbar_wait(&S.full[s], (uint32_t)((fills[s] - 1) & 1)))
+                    if (fills[s] > 0 && !mbar_drain(&S.full[s], (uint32_t)((fills[s] - 1) & 1)))
                         atomicOr(P.status, kStatusTimeout);
             }
         } else if (warp == kWarpMma) {
@@ -409,13 +417,27 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
                 WAIT_OR_ABORT(&S.full[s], (uint32_t)((i / kStages) & 1));
                 // X[i % 2] still holds the outputs of chunk i - 2 until they are read
                 if (i >= 2) WAIT_OR_ABORT(&S.x_free[i & 1], (uint32_t)(((i - 2) >> 1) & 1));
-                WAIT_OR_ABORT(&S.s_ready, ph);
+                // MMA1 in two halves: the K-steps of snapshot round 0 (key channels
+                // 0-31 and 64-95) as soon as it lands, then those of round 1
+                WAIT_OR_ABORT(&S.s_ready[0], ph);
                 tc_fence_after();
                 if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
+                    for (int j = 0; j < 4; ++j) {
+                        const int kk = (j & 1) + 4 * (j >> 1);  // 0, 1, 4, 5
                         mma_bf16_ta(tX, tbase + kColSb + 8 * kk, dWQ0 + so + 16u * kk, idesc1,
-                                    kk > 0 ? 1u : 0u);
+                                    j > 0 ? 1u : 0u);
+                    }
+                }
+                __syncwarp();
+                WAIT_OR_ABORT(&S.s_ready[1], ph);
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int kk = 2 + (j & 1) + 4 * (j >> 1);  // 2, 3, 6, 7
+                        mma_bf16_ta(tX, tbase + kColSb + 8 * kk, dWQ0 + so + 16u * kk, idesc1, 1u);
+                    }
                     mma_commit(&S.mma1);
                 }
                 __syncwarp();
@@ -440,6 +462,12 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
                 }
                 __syncwarp();
             }
+            // every MMA issued above has completed before TMEM is freed (after
+            // a normal end the consumers already waited for them; after giving
+            // up some may still be running)
+            if (elect_one()) mma_commit(&S.mma_done);
+            __syncwarp();
+            if (!mbar_drain(&S.mma_done, 0)) atomicOr(P.status, kStatusTimeout);
         } else {
             // ---------------------------------------------------- output warps
             const int q = warp & 3;          // TMEM lane quarter

@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) seg_scan_kernel(const ScanArg
     if (threadIdx.x == 0) s_abort = (*((volatile int*)A.status) & kStatusTimeout) ? 1 : 0;
     __syncthreads();
     if (s_abort) return;
+    const uint64_t lim = wait_limit_ns(A.status);  // of the copy waits that may give up
 
     const int H = A.H, P = A.P;
     const int slice = blockIdx.x % kScanSlices;
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) seg_scan_kernel(const ScanArg
             x_next = *reinterpret_cast<const float4*>(maps_of(j + 1) + (size_t)r * kDim + c);
         *reinterpret_cast<float4*>(A.start + (((size_t)n * P + j) * H + h) * KK +
                                    (size_t)r * kDim + c) = s;
-        if (!mbar_wait(&bar[b], (uint32_t)((j >> 1) & 1))) {
+        if (!mbar_wait(&bar[b], (uint32_t)((j >> 1) & 1), lim)) {
             atomicOr(A.status, kStatusTimeout);
             s_abort = 1;
         }
@@ -147,11 +148,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) seg_scan_kernel(const ScanArg
         __syncthreads();  // S_{j+1} visible
     }
     if (j < P) {
-        // gave up: wait once more (bounded) for the copy step j timed out on and
-        // for the one issued in step j before leaving
+        // gave up: wait once more, with the longer drain limit, for the copy
+        // step j timed out on and for the one issued in step j before leaving
         if (t == 0) {
-            mbar_wait(&bar[j & 1], (uint32_t)((j >> 1) & 1));
-            if (j + 1 < P) mbar_wait(&bar[(j + 1) & 1], (uint32_t)(((j + 1) >> 1) & 1));
+            mbar_drain(&bar[j & 1], (uint32_t)((j >> 1) & 1));
+            if (j + 1 < P) mbar_drain(&bar[(j + 1) & 1], (uint32_t)(((j + 1) >> 1) & 1));
         }
         return;
     }
@@ -186,6 +187,10 @@ int segment_count(int64_t N, int64_t H, int64_t max_chunks, int kind) {
         if (by_len < P) P = by_len;
         return P >= kMinSegments ? (int)P : 0;
     }
+    // forced: with more (sequence, head) pairs than half the SMs the segments
+    // would not run side by side and their states (192 KB per segment and
+    // head) would only cost memory, so the unsplit path runs instead
+    if (fill == 0) return 0;
     const int64_t by_len = per_seq / 2;
     if (by_len < P) P = by_len;
     return P >= 2 ? (int)P : 2;

@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(128, 1)
             }
             mma_commit(&bar);
         }
-        if (!mbar_wait(&bar, (uint32_t)(combo & 1))) {
+        if (!mbar_drain(&bar, (uint32_t)(combo & 1))) {
             ok = false;
             atomicOr(status, 1);
         }

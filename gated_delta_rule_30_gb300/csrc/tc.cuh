@@ -72,17 +72,53 @@ __device__ __forceinline__ uint64_t global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+__device__ __forceinline__ uint32_t mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok;
+}
+
+// Limits below this are test settings (kda_set_wait_limit_ns): such a wait
+// polls without suspending, so that any wait that does not complete at once
+// gives up, whatever the hardware's suspend time of try_wait.
+constexpr uint64_t kShortWaitNs = 1000000ull;
+
 // Wait for the phase with the given parity to complete.  Bounded: returns
 // false (and the caller must report a timeout and unwind) after `limit_ns`.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          uint64_t limit_ns = 2000000000ull) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The retry loop is kept rolled: it is inlined at every wait, and unrolled
+// copies cost instruction-cache misses in the large fused kernel (measured).
+// All lanes of a converged warp read the barrier and the global timer in the
+// same instructions, so they return the same answer.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    const bool poll = limit_ns < kShortWaitNs;
+    if (!poll && mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > limit_ns) return false;
+#pragma unroll 1
+    for (uint32_t i = 1;; ++i) {
+        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if ((i & 15u) == 0 && global_ns() - t0 > limit_ns) return false;
     }
+}
+
+// The library's per-device status block (kda_api.cu): word 0 holds the status
+// bits, words 2-3 the limit in ns of the bounded waits that can give up on the
+// way (2 s unless kda_set_wait_limit_ns changed it).  Kernels read it once, at
+// the start.
+__device__ __forceinline__ uint64_t wait_limit_ns(const int* status) {
+    return *reinterpret_cast<const volatile unsigned long long*>(status + 2);
+}
+// Limit of the waits a CTA makes for its own copies and MMAs before it exits
+// after giving up: longer than any limit a caller sets, so that nothing the CTA
+// started is still writing its shared or tensor memory when it leaves.
+constexpr uint64_t kDrainLimitNs = 4000000000ull;
+// Wait (bounded by kDrainLimitNs) for the phase; used only to drain.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+    return mbar_wait(bar, parity, kDrainLimitNs);
 }
 
 // ----------------------------------------------------------------------------- bulk copies

@@ -17,7 +17,8 @@
  *     S_t  = (I - beta_t k_t k_t^T) Diag(exp(la_t)) S_{t-1} + beta_t k_t v_t^T
  *     o_t  = scale * S_t^T q_t
  * S_0 = initial_state[n, h] (or 0); final_state[n, h] = S at the sequence end.
- * q and k are used as given (no normalisation inside the call).
+ * q and k are used as given (no normalisation inside the call); kda_fwd_ex
+ * can normalise them first.
  *
  * Every pointer handed to kda_fwd is DEVICE memory owned by the caller; the
  * call reads the inputs, writes out (and final_state) and keeps no reference
@@ -100,7 +101,9 @@ kda_status_t kda_fwd(const void* q, const void* k, const void* v, const void* g,
  * problem with these sizes (an upper bound that does not read cu_seqlens),
  * for the recurrence selection in force (kda_set_recurrence_kernel: the
  * segmented path needs room for its per-segment states, so query the size
- * after choosing).  Returns 0 and sets the error message for invalid sizes.
+ * after choosing).  A problem that takes the single-token step (T = 1 without
+ * cu_seqlens, automatic selection) uses no scratch: the answer is then 256.
+ * Returns 0 and sets the error message for invalid sizes.
  */
 size_t kda_workspace_size(int32_t B, int32_t T, int32_t H, int32_t num_seqs, int32_t has_cu_seqlens);
 
@@ -118,6 +121,30 @@ kda_status_t kda_fwd_ws(const void* q, const void* k, const void* v, const void*
                         int32_t H, int32_t K, int32_t V, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/* kda_fwd_ex flag: scale every row of q and k (one token of one head, K
+ * channels) to x / sqrt(sum_c x_c^2 + 1e-6) inside the kernels before use. */
+#define KDA_FWD_QK_L2NORM 1u
+
+/*
+ * kda_fwd_ex -- kda_fwd with options.  The call printed in "Flashkda Delta
+ * Attention", "Core Kernel API", takes q and k as given; callers that hold
+ * raw (un-normalised) query/key projections would otherwise run a separate
+ * normalisation pass over q and k in HBM first.  With KDA_FWD_QK_L2NORM the
+ * chunk kernel (and the single-token step) normalise each row of the staged
+ * q / k tiles instead; the normalised rows are rounded to bf16 like the
+ * inputs before use.  `flags`: 0 or KDA_FWD_QK_L2NORM (other bits return
+ * KDA_ERR_INVALID_ARGUMENT).  `workspace`: as for kda_fwd_ws, or NULL to take
+ * scratch from the stream-ordered allocator as kda_fwd does (then
+ * workspace_bytes is ignored).  Same arguments and errors as kda_fwd otherwise.
+ */
+kda_status_t kda_fwd_ex(const void* q, const void* k, const void* v, const void* g,
+                        const void* beta, float scale, void* out, const float* A_log,
+                        const float* dt_bias, float lower_bound, const void* initial_state,
+                        kda_dtype_t initial_dtype, void* final_state, kda_dtype_t final_dtype,
+                        const int32_t* cu_seqlens, int32_t num_seqs, int32_t B, int32_t T,
+                        int32_t H, int32_t K, int32_t V, uint32_t flags, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
 /*
  * kda_fwd_noalloc -- kda_fwd for callers that must not allocate device memory
  * during the call (no counterpart on the pages).  Some callers cannot: a
@@ -129,7 +156,10 @@ kda_status_t kda_fwd_ws(const void* q, const void* k, const void* v, const void*
  * loads the library holds until the process exits.  Inputs and outputs are
  * the caller's, exactly as for kda_fwd.
  *   - A problem whose kda_workspace_size exceeds the area is rejected with
- *     KDA_ERR_UNSUPPORTED and a message giving both sizes.
+ *     KDA_ERR_UNSUPPORTED and a message giving both sizes.  Single-token
+ *     problems (T = 1 without cu_seqlens, automatic recurrence selection)
+ *     take the single-token step, which uses no scratch, so every batch size
+ *     of them is accepted.
  *   - The first call on a device looks up the area's address on that device
  *     (it must be the current device); make that first call before any stream
  *     capture.
@@ -206,11 +236,30 @@ kda_status_t kda_set_stage_events(void* const* events, int32_t count);
  * split into 2..32 segments; the affine state map of every segment is found
  * in parallel, the maps are scanned in fp32, and the value-sliced recurrence
  * then runs all segments at once from their entering states; automatic
- * selection takes it for few, long sequences).  Process-wide, applies to
- * later calls, including kda_workspace_size; not thread-safe.  Any other kind
- * returns KDA_ERR_INVALID_ARGUMENT.
+ * selection takes it for few, long sequences; forced, it falls back to the
+ * kind-0 choice between 1 and 2 when the (sequence, head) pairs exceed half
+ * the SM count, where the segments could not run side by side).  Process-wide
+ * (an atomic setting, safe to change from any thread): it applies to calls
+ * that start after it returns, including kda_workspace_size, so a caller that
+ * sizes a workspace must not change it between the query and the call.  Any
+ * other kind returns KDA_ERR_INVALID_ARGUMENT.
  */
 kda_status_t kda_set_recurrence_kernel(int32_t kind);
+
+/*
+ * kda_set_wait_limit_ns -- test hook (no counterpart on the pages).  Every
+ * device-side wait of the kernels that can give up (an mbarrier wait for a
+ * copy or an MMA, or the fused launch's wait for a chunk record) is bounded by
+ * this limit, 2e9 ns (2 s) by default.  A wait that runs out records
+ * KDA_ERR_TIMEOUT in the status word (see kda_device_status), the CTA stops,
+ * waits for its own copies and MMAs in flight (with a separate 4 s limit),
+ * frees its tensor memory and exits, and later CTAs of the launch exit at
+ * once.  A short limit makes that path run on purpose; the outputs of a call
+ * that timed out are undefined, and the next call is unaffected.
+ * limit_ns in [1, 2e9]; applies to the current device and to kernels
+ * launched after the call (it writes a word of the device's status block).
+ */
+kda_status_t kda_set_wait_limit_ns(uint64_t limit_ns);
 
 /*
  * kda_selftest_tcgen05 -- diagnostic for the tensor-core building blocks the

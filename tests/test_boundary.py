@@ -147,3 +147,34 @@ def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(kda, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         kda.lib()
+
+
+def test_fwd_ex_rejects_unknown_flags(kda_lib):
+    """kda_fwd_ex: flag bits other than KDA_FWD_QK_L2NORM are an argument error,
+    and its other arguments are validated like kda_fwd's (nothing launched)."""
+    L = kda_lib.lib()
+
+    def ex(flags, K=128):
+        rc = L.kda_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 0.088, FAKE, FAKE, FAKE, -5.0, None, 0,
+                          None, 0, None, 0, 1, 64, 2, K, 128, flags, None, 0, None)
+        return rc, L.kda_last_error_message().decode()
+
+    for bad in (2, 4, 0x80000000, 3):
+        rc, msg = ex(bad)
+        assert rc == 1 and "flag" in msg, (bad, rc, msg)
+    rc, msg = ex(1, K=64)   # a valid flag does not skip the shape checks
+    assert rc == 1 and "128" in msg
+
+
+def test_workspace_size_single_token_step(kda_lib):
+    """Single-token problems take the step that uses no scratch: the answer is the
+    minimum (256 bytes) under automatic selection, the chunked size otherwise."""
+    L = kda_lib.lib()
+    try:
+        kda_lib.set_recurrence_kernel("auto")
+        assert L.kda_workspace_size(1024, 1, 32, 0, 0) == 256
+        assert L.kda_workspace_size(1, 1024, 32, 1024, 1) > 256   # packed: chunked path
+        kda_lib.set_recurrence_kernel("transposed")
+        assert L.kda_workspace_size(1024, 1, 32, 0, 0) > 64 << 20
+    finally:
+        kda_lib.set_recurrence_kernel("auto")

@@ -65,6 +65,22 @@ def test_noalloc_matches_allocating_entry_twice(kda_lib):
         assert_close(hT.double(), ref_hT.double().numpy(), f"{w.name} final_state")
 
 
+@pytest.mark.gpu
+def test_noalloc_single_token_batches_of_any_size(kda_lib):
+    """A decoding step of 1024 sequences x 32 heads (T = 1): the single-token step
+    uses no scratch, so the entry point accepts it and gives the same bits as the
+    allocating entry point (the same kernel runs)."""
+    kda_lib.set_recurrence_kernel("auto")
+    L = _noalloc(kda_lib)
+    assert L.kda_workspace_size(1024, 1, 32, 0, 0) <= L.kda_noalloc_scratch_bytes()
+    p = inputs.make(inputs.WORKLOADS["decode"])
+    ref_out, ref_hT = run_gpu(p)
+    for _ in range(2):
+        out, hT = _run_noalloc(kda_lib, p)
+        assert kda_lib.last_path() == "decode"
+        assert torch.equal(out, ref_out) and torch.equal(hT, ref_hT)
+
+
 def test_noalloc_rejects_problems_above_the_area(kda_lib):
     L = _noalloc(kda_lib)
     limit = L.kda_noalloc_scratch_bytes()
