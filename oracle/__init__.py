@@ -71,6 +71,10 @@ def lib():
                                           _fp, ctypes.c_double, ctypes.c_void_p, ctypes.c_int, _dp,
                                           _dp, _i64p, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
+        L.kda_oracle_bwd_f64.restype = ctypes.c_int
+        L.kda_oracle_bwd_f64.argtypes = ([_dp] * 5 + [ctypes.c_double, _dp, _dp, ctypes.c_double]
+                                         + [_dp] * 3 + [_i64p] + [ctypes.c_int64] * 4
+                                         + [_dp] * 8 + [ctypes.c_int])
         L.kda_oracle_chunk.restype = ctypes.c_int
         L.kda_oracle_chunk.argtypes = [_dp, ctypes.c_int64, _dp, ctypes.c_int64, _dp,
                                        ctypes.c_int64, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
@@ -219,6 +223,39 @@ def recurrent(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_stat
     if rc:
         raise ValueError(f"kda_oracle_fwd failed ({rc})")
     return out.reshape(tuple(v.shape[:-1]) + (V,)), hT
+
+
+def recurrent_bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout,
+                  initial_state=None, dfinal_state=None, cu_seqlens=None, nthreads=0):
+    """Reverse mode of ``recurrent`` (fp64): gradients of
+    L = sum(dout * out) + sum(dfinal_state * final_state).
+
+    Shapes as for ``recurrent``; dout is shaped like v, dfinal_state like the
+    state [N, H, K, V] (None: no final-state term).  Returns a dict with dq, dk,
+    dv, dg, dbeta (shaped like the inputs), dA_log [H], ddt_bias [H, K] and dh0
+    [N, H, K, V], all float64.
+    """
+    B, T = _bt(q)
+    cu = _cu(cu_seqlens, B, T)
+    N = len(cu) - 1
+    H, K = q.shape[-2], q.shape[-1]
+    V = v.shape[-1]
+    qf, kf, vf, gf, bf = (_f64(x) for x in (q, k, v, g, beta))
+    h0 = _f64(initial_state)
+    do = _f64(dout)
+    dhT = _f64(dfinal_state)
+    res = {"dq": np.empty_like(qf), "dk": np.empty_like(kf), "dv": np.empty_like(vf),
+           "dg": np.empty_like(gf), "dbeta": np.empty_like(bf), "dA_log": np.empty(H),
+           "ddt_bias": np.empty((H, K)), "dh0": np.empty((N, H, K, V))}
+    rc = lib().kda_oracle_bwd_f64(_ptr(qf), _ptr(kf), _ptr(vf), _ptr(gf), _ptr(bf), float(scale),
+                                  _ptr(_f64(A_log)), _ptr(_f64(dt_bias)), float(lower_bound),
+                                  _ptr(h0), _ptr(do), _ptr(dhT), _ptr(cu, _i64p), N, H, K, V,
+                                  *(_ptr(res[n]) for n in ("dq", "dk", "dv", "dg", "dbeta",
+                                                           "dA_log", "ddt_bias", "dh0")),
+                                  int(nthreads))
+    if rc:
+        raise ValueError(f"kda_oracle_bwd_f64 failed ({rc})")
+    return res
 
 
 def chunked(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state=None,

@@ -401,3 +401,221 @@ int kda_oracle_gate(const double* g, int64_t n_tok, int64_t H, int64_t K, const 
             }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------------
+ * Reverse mode of the token-by-token recurrence (the backward pass).
+ *
+ * The pages describe the forward call only (and recommend running it under
+ * torch.inference_mode, "MoonshotAI/FlashKDA", "Automatic Branching for
+ * Installation and Usage"); the gradients below are those of the recurrence
+ * defined at the top of this file, taken by the chain rule step by step in
+ * reverse token order.  For one (sequence, head), with the scalar loss
+ * L = sum_t <dout_t, o_t> + <dhT, S_final>, per token t (forward quantities as
+ * in recur_one: x, sp = softplus(x), pre = -exp(A_log) sp, la = max(pre, lb),
+ * alpha = exp(la), St = Diag(alpha) S_{t-1}, r = St^T k, u = beta (v - r),
+ * S_t = St + k u^T, o_t = scale S_t^T q):
+ *
+ *   dS  += scale q dout_t^T            dq   = scale S_t dout_t
+ *   dk  += dS u                         du   = dS^T k          (dSt = dS)
+ *   dbeta = <du, v - r>                dv   = beta du          dr = -beta du
+ *   dSt += k dr^T                       dk  += St dr
+ *   dalpha_c = sum_j dSt[c][j] S_{t-1}[c][j]                   dS_{t-1} = Diag(alpha) dSt
+ *   dla = dalpha alpha;  dpre = dla where pre >= lb, else 0   (the max passes its
+ *                        gradient to the argument it returns; at a tie, to pre)
+ *   dA_log += sum_c pre_c dpre_c        dsp = -exp(A_log) dpre
+ *   dx  = dsp sigmoid(x)                dg = dx, ddt_bias += dx
+ *
+ * and dh0 = dS after the first token.  The forward states S_0 .. S_L of the
+ * sequence are kept (L + 1 matrices of K x V doubles), so this is meant for the
+ * small problems of the test-suite.
+ * ------------------------------------------------------------------------------ */
+
+static double sigmoid(double x) {
+    if (x >= 0.0) return 1.0 / (1.0 + exp(-x));
+    const double e = exp(x);
+    return e / (1.0 + e);
+}
+
+typedef struct {
+    const double *q, *k, *v, *g, *beta, *A_log, *dt_bias, *h0, *dout, *dhT;
+    double scale, lower_bound;
+    double *dq, *dk, *dv, *dg, *dbeta, *dA_log, *ddt_bias, *dh0;
+    const int64_t* cu;
+    int64_t N, H, K, V;
+} grad_problem_t;
+
+/* One (sequence, head).  dA_log_h and ddt_bias_h are this pair's private
+ * accumulators (the caller sums them over sequences). */
+static int grad_one(const grad_problem_t* P, int64_t n, int64_t h, double* dA_log_h,
+                    double* ddt_bias_h) {
+    const int64_t K = P->K, V = P->V, H = P->H, KV = K * V;
+    const int64_t t0 = P->cu[n], L = P->cu[n + 1] - P->cu[n];
+    const double a = exp(P->A_log[h]);
+    double* Ss = (double*)malloc(sizeof(double) * (size_t)((L + 1) * KV));
+    double* work = (double*)malloc(sizeof(double) * (size_t)(2 * KV + 6 * V + 4 * K));
+    if (!Ss || !work) {
+        free(Ss);
+        free(work);
+        return ORACLE_ENOMEM;
+    }
+    double* dS = work;
+    double* St = dS + KV;
+    double* r = St + KV;
+    double* u = r + V;
+    double* du = u + V;
+    double* dr = du + V;
+    double* tmp = dr + V;
+    double* spare = tmp + V;
+    double* alpha = spare + V;
+    double* pre = alpha + K;
+    double* xg = pre + K;
+    double* dal = xg + K;
+    (void)spare;
+
+    /* forward: S_0 = h0, S_{t+1} after token t */
+    for (int64_t i = 0; i < KV; ++i) Ss[i] = P->h0 ? P->h0[(n * H + h) * KV + i] : 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+        const int64_t row = (t0 + t) * H + h;
+        const double* S0 = Ss + t * KV;
+        double* S1 = Ss + (t + 1) * KV;
+        for (int64_t c = 0; c < K; ++c) {
+            const double x = P->g[row * K + c] + P->dt_bias[h * K + c];
+            double la = -a * softplus(x);
+            if (la < P->lower_bound) la = P->lower_bound;
+            for (int64_t j = 0; j < V; ++j) S1[c * V + j] = exp(la) * S0[c * V + j];
+        }
+        for (int64_t j = 0; j < V; ++j) r[j] = 0.0;
+        for (int64_t c = 0; c < K; ++c)
+            for (int64_t j = 0; j < V; ++j) r[j] += S1[c * V + j] * P->k[row * K + c];
+        const double b = P->beta[row];
+        for (int64_t j = 0; j < V; ++j) u[j] = b * (P->v[row * V + j] - r[j]);
+        for (int64_t c = 0; c < K; ++c)
+            for (int64_t j = 0; j < V; ++j) S1[c * V + j] += P->k[row * K + c] * u[j];
+    }
+
+    /* backward */
+    for (int64_t i = 0; i < KV; ++i) dS[i] = P->dhT ? P->dhT[(n * H + h) * KV + i] : 0.0;
+    for (int64_t t = L - 1; t >= 0; --t) {
+        const int64_t row = (t0 + t) * H + h;
+        const double* Sprev = Ss + t * KV;
+        const double* Scur = Ss + (t + 1) * KV;
+        const double* qv = P->q + row * K;
+        const double* kv = P->k + row * K;
+        const double* vv = P->v + row * V;
+        const double* dov = P->dout + row * V;
+        const double b = P->beta[row];
+        /* recompute the token's forward quantities */
+        for (int64_t c = 0; c < K; ++c) {
+            xg[c] = P->g[row * K + c] + P->dt_bias[h * K + c];
+            pre[c] = -a * softplus(xg[c]);
+            const double la = pre[c] < P->lower_bound ? P->lower_bound : pre[c];
+            alpha[c] = exp(la);
+            for (int64_t j = 0; j < V; ++j) St[c * V + j] = alpha[c] * Sprev[c * V + j];
+        }
+        for (int64_t j = 0; j < V; ++j) r[j] = 0.0;
+        for (int64_t c = 0; c < K; ++c)
+            for (int64_t j = 0; j < V; ++j) r[j] += St[c * V + j] * kv[c];
+        for (int64_t j = 0; j < V; ++j) u[j] = b * (vv[j] - r[j]);
+        /* o_t = scale S_t^T q */
+        for (int64_t c = 0; c < K; ++c) {
+            double s = 0.0;
+            for (int64_t j = 0; j < V; ++j) {
+                dS[c * V + j] += P->scale * qv[c] * dov[j];
+                s += Scur[c * V + j] * dov[j];
+            }
+            P->dq[row * K + c] = P->scale * s;
+        }
+        /* S_t = St + k u^T */
+        for (int64_t j = 0; j < V; ++j) du[j] = 0.0;
+        for (int64_t c = 0; c < K; ++c) {
+            double s = 0.0;
+            for (int64_t j = 0; j < V; ++j) {
+                s += dS[c * V + j] * u[j];
+                du[j] += dS[c * V + j] * kv[c];
+            }
+            P->dk[row * K + c] = s;
+        }
+        /* u = beta (v - r) */
+        double db = 0.0;
+        for (int64_t j = 0; j < V; ++j) {
+            db += du[j] * (vv[j] - r[j]);
+            P->dv[row * V + j] = b * du[j];
+            dr[j] = -b * du[j];
+        }
+        P->dbeta[row] = db;
+        /* r = St^T k: dSt = dS + k dr^T, dk += St dr */
+        for (int64_t c = 0; c < K; ++c) {
+            double s = 0.0;
+            for (int64_t j = 0; j < V; ++j) {
+                s += St[c * V + j] * dr[j];
+                dS[c * V + j] += kv[c] * dr[j];
+            }
+            P->dk[row * K + c] += s;
+        }
+        /* St = Diag(alpha) S_{t-1} */
+        for (int64_t c = 0; c < K; ++c) {
+            double s = 0.0;
+            for (int64_t j = 0; j < V; ++j) {
+                s += dS[c * V + j] * Sprev[c * V + j];
+                dS[c * V + j] *= alpha[c];
+            }
+            dal[c] = s;
+        }
+        /* gate */
+        for (int64_t c = 0; c < K; ++c) {
+            const double dla = dal[c] * alpha[c];
+            const double dpre = pre[c] >= P->lower_bound ? dla : 0.0;
+            *dA_log_h += pre[c] * dpre;
+            const double dx = -a * dpre * sigmoid(xg[c]);
+            P->dg[row * K + c] = dx;
+            ddt_bias_h[c] += dx;
+        }
+    }
+    if (P->dh0)
+        for (int64_t i = 0; i < KV; ++i) P->dh0[(n * H + h) * KV + i] = dS[i];
+    free(Ss);
+    free(work);
+    return ORACLE_OK;
+}
+
+/*
+ * Gradients of L = sum <dout, out> + <dhT, final_state> with respect to every
+ * input of kda_oracle_fwd_f64 (erase = 1).  Layouts as for the forward; dhT,
+ * h0 and dh0 may be NULL (no final-state gradient / zero initial state / not
+ * wanted).  dA_log [H] and ddt_bias [H, K] are sums over all tokens.
+ */
+int kda_oracle_bwd_f64(const double* q, const double* k, const double* v, const double* g,
+                       const double* beta, double scale, const double* A_log,
+                       const double* dt_bias, double lower_bound, const double* h0,
+                       const double* dout, const double* dhT, const int64_t* cu, int64_t N,
+                       int64_t H, int64_t K, int64_t V, double* dq, double* dk, double* dv,
+                       double* dg, double* dbeta, double* dA_log, double* ddt_bias, double* dh0,
+                       int nthreads) {
+    if (N < 0 || H <= 0 || K <= 0 || V <= 0 || !cu || cu[0] != 0) return ORACLE_EINVAL;
+    for (int64_t n = 0; n < N; ++n)
+        if (cu[n + 1] < cu[n]) return ORACLE_EINVAL;
+    grad_problem_t P = {q, k, v, g, beta, A_log, dt_bias, h0, dout, dhT, scale, lower_bound,
+                        dq, dk, dv, dg, dbeta, dA_log, ddt_bias, dh0, cu, N, H, K, V};
+    const int64_t pairs = N * H;
+    double* acc = (double*)calloc((size_t)(pairs * (K + 1)), sizeof(double));
+    if (!acc) return ORACLE_ENOMEM;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+#endif
+    for (int64_t p = 0; p < pairs; ++p)
+        failed |= grad_one(&P, p / H, p % H, acc + p * (K + 1), acc + p * (K + 1) + 1);
+    /* per-head sums over the sequences, in a fixed order */
+    for (int64_t h = 0; h < H; ++h) {
+        dA_log[h] = 0.0;
+        for (int64_t c = 0; c < K; ++c) ddt_bias[h * K + c] = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            const double* ac = acc + (n * H + h) * (K + 1);
+            dA_log[h] += ac[0];
+            for (int64_t c = 0; c < K; ++c) ddt_bias[h * K + c] += ac[1 + c];
+        }
+    }
+    free(acc);
+    return failed ? ORACLE_ENOMEM : ORACLE_OK;
+}

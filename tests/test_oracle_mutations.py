@@ -16,6 +16,7 @@ import pytest
 
 import oracle
 import test_oracle as pins
+import test_oracle_bwd as bwd_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "kda_oracle.c")
 
@@ -54,6 +55,14 @@ MUTATIONS = [
      "const double inv = 1.0 / (ss + eps);"),
     ("l2norm over the first channel only", "for (int64_t c = 0; c < D; ++c) ss += row[c] * row[c];",
      "for (int64_t c = 0; c < 1; ++c) ss += row[c] * row[c];"),
+    ("bwd: sign of the erase-key gradient", "dr[j] = -b * du[j];", "dr[j] = b * du[j];"),
+    ("bwd: decay not carried back", "dS[c * V + j] *= alpha[c];", "dS[c * V + j] *= 1.0;"),
+    ("bwd: clamp mask inverted", "const double dpre = pre[c] >= P->lower_bound ? dla : 0.0;",
+     "const double dpre = pre[c] >= P->lower_bound ? 0.0 : dla;"),
+    ("bwd: softplus derivative dropped", "const double dx = -a * dpre * sigmoid(xg[c]);",
+     "const double dx = -a * dpre;"),
+    ("bwd: dq from the state before the write", "s += Scur[c * V + j] * dov[j];",
+     "s += St[c * V + j] * dov[j];"),
 ]
 
 PINS = [
@@ -76,6 +85,11 @@ PINS = [
     ("l2norm closed form", pins.test_l2norm_closed_form),
     ("l2norm scale-free rows", pins.test_l2norm_is_scale_free_per_row),
     ("l2norm vs brute force", pins.test_l2norm_matches_brute_force),
+    ("bwd directional lb=-3", lambda m: bwd_pins.test_directional_derivatives(m, -3.0)),
+    ("bwd directional lb=-0.6", lambda m: bwd_pins.test_directional_derivatives(m, -0.6)),
+    ("bwd elementwise Jacobian", bwd_pins.test_jacobian_elementwise_tiny),
+    ("bwd beta = 0 closed form", bwd_pins.test_beta_zero_closed_form),
+    ("bwd all clamped", bwd_pins.test_all_clamped_gate_has_no_gradient),
 ]
 
 
