@@ -41,8 +41,8 @@
 // products (M = 128 channels, N = 64 tokens,
 // K = 64 tokens) run on tcgen05 with fp32 accumulators in TMEM.  The
 // triangular inverse is blocked: the four 16 x 16 diagonal blocks by forward
-// substitution (one warp each), then the off-diagonal blocks level by level,
-// T_ab = -T_aa sum_{b<=c<a} A_ac T_cb, in fp32 shared memory.
+// substitution (two warps), then the off-diagonal blocks by 2 x 2 block
+// recursion (T_10, T_32, then the lower-left 32 x 32 block), in fp32 shared memory.
 #pragma once
 #include <cuda.h>  // CUtensorMap (the encoder is fetched at run time)
 #include <cuda_runtime.h>
@@ -69,7 +69,7 @@ constexpr uint32_t kSmBytes = 106496;
 constexpr int kStr = 68;              // fp32 row stride of the 64 x 64 tiles
 constexpr uint32_t kSmA = 0;          // A^T (beta-scaled, strictly lower A), fp32 [64][kStr]
 constexpr uint32_t kSmT = 17408;      // T, fp32 [64][kStr]
-constexpr uint32_t kSmX = 34816;      // level products, fp32 [3][16][16]
+constexpr uint32_t kSmX = 34816;      // products of the inverse's recursion, fp32 (<= 32 x kXb)
 constexpr uint32_t kSmTT = 40960;     // T^T as MN-major B operand, bf16 8 KB
 // R_a (16(a+1) rows x 256 B) starts at 2048 a (a+1): 0, 4096, 12288, 24576
 __host__ __device__ constexpr uint32_t r_off(int a) { return 2048u * a * (a + 1); }
@@ -196,49 +196,86 @@ __device__ __forceinline__ void st_release_gpu(int* p, int v) {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Off-diagonal blocks of T = (I + A)^-1 at block distance D (16 x 16 blocks,
-// a = b + D):  X_ab = sum_{c=b}^{a-1} A_ac T_cb,  T_ab = -T_aa X_ab.  Each of
-// the first (4 - D) * 64 threads computes a 2 x 2 tile (rows r, r+1; columns
-// c, c+1) of one block; the trip counts are compile-time constants.
-template <int D>
-__device__ __forceinline__ void level_products(const float* sAT, float* sT, float* sX, int tid,
-                                               uint32_t bar_id) {
-    constexpr int kItems = (4 - D) * 64;
-    const int b = tid >> 6, r = ((tid >> 3) & 7) * 2, c = (tid & 7) * 2;
-    const int a = b + D;
-    if (tid < kItems) {
+// Off-diagonal part of T = (I + A)^-1 from its four diagonal 16 x 16 blocks
+// (already in sT), by 2 x 2 block recursion on all kThreads threads:
+//   T_10 = -T_11 A_10 T_00  and  T_32 = -T_33 A_32 T_22   (steps A1, A2), after
+//   which T_lo = T[0:32][0:32] and T_hi = T[32:64][32:64] are the inverses of
+//   the two diagonal halves, then
+//   T[32:64][0:32] = -T_hi A[32:64][0:32] T_lo             (steps B1, B2).
+// In B1 each warp owns four columns j and sums only c >= its first column (T_lo
+// is lower triangular); in B2 each warp owns four rows i and sums only c <= its
+// last row (T_hi is lower triangular).  sAT[l][i] = A[i][l]; sX is scratch.
+constexpr int kXs = 18;   // row stride of the 16 x 16 products in sX
+constexpr int kXb = 34;   // row stride of the 32 x 32 product in sX
+__device__ __forceinline__ void offdiag_inverse(const float* sAT, float* sT, float* sX, int tid,
+                                                uint32_t bar_id) {
+    const int warp = tid >> 5, lane = tid & 31;
+    {
+        // A1: X = A_ab T_bb for (a, b) = (1, 0) (threads 0-127) and (3, 2) (128-255);
+        // thread: row i, columns j, j + 1
+        const int blk = tid >> 7, i = tid & 15, j = ((tid >> 4) & 7) * 2;
+        const int r0 = 16 + 32 * blk, c0 = 32 * blk;
+        float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const float av = sAT[(c0 + c) * kStr + r0 + i];
+            const float2 tv = *reinterpret_cast<const float2*>(sT + (c0 + c) * kStr + c0 + j);
+            x0 = fmaf(av, tv.x, x0);
+            x1 = fmaf(av, tv.y, x1);
+        }
+        *reinterpret_cast<float2*>(sX + blk * 16 * kXs + i * kXs + j) = make_float2(x0, x1);
+    }
+    sub_sync(bar_id);
+    {
+        // A2: T_ab = -T_aa X; thread: rows i, i + 1, column j
+        const int blk = tid >> 7, j = tid & 15, i = ((tid >> 4) & 7) * 2;
+        const int r0 = 16 + 32 * blk, c0 = 32 * blk;
+        float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const float xv = sX[blk * 16 * kXs + c * kXs + j];
+            y0 = fmaf(sT[(r0 + i) * kStr + r0 + c], xv, y0);
+            y1 = fmaf(sT[(r0 + i + 1) * kStr + r0 + c], xv, y1);
+        }
+        sT[(r0 + i) * kStr + c0 + j] = -y0;
+        sT[(r0 + i + 1) * kStr + c0 + j] = -y1;
+    }
+    sub_sync(bar_id);
+    {
+        // B1: X = A[32:64][0:32] T_lo; warp w: columns 4w .. 4w + 3 (lanes 16-31 the
+        // upper pair), rows 2 (lane % 16) and + 1
+        const int i = (lane & 15) * 2, j = 4 * warp + 2 * (lane >> 4);
         float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
-        const float* ap = sAT + 16 * b * kStr + 16 * a + r;
-        const float* tp = sT + 16 * b * kStr + 16 * b + c;
-#pragma unroll 8
-        for (int l = 0; l < 16 * D; ++l) {
-            const float2 av = *reinterpret_cast<const float2*>(ap + l * kStr);
-            const float2 tv = *reinterpret_cast<const float2*>(tp + l * kStr);
+#pragma unroll 4
+        for (int c = 4 * warp; c < 32; ++c) {
+            const float2 av = *reinterpret_cast<const float2*>(sAT + c * kStr + 32 + i);
+            const float2 tv = *reinterpret_cast<const float2*>(sT + c * kStr + j);
             x00 = fmaf(av.x, tv.x, x00);
             x01 = fmaf(av.x, tv.y, x01);
             x10 = fmaf(av.y, tv.x, x10);
             x11 = fmaf(av.y, tv.y, x11);
         }
-        *reinterpret_cast<float2*>(sX + b * 256 + r * 16 + c) = make_float2(x00, x01);
-        *reinterpret_cast<float2*>(sX + b * 256 + (r + 1) * 16 + c) = make_float2(x10, x11);
+        *reinterpret_cast<float2*>(sX + i * kXb + j) = make_float2(x00, x01);
+        *reinterpret_cast<float2*>(sX + (i + 1) * kXb + j) = make_float2(x10, x11);
     }
     sub_sync(bar_id);
-    if (tid < kItems) {
+    {
+        // B2: T[32:64][0:32] = -T_hi X; warp w: rows 4w .. 4w + 3 (lanes 16-31 the
+        // upper pair), columns 2 (lane % 16) and + 1
+        const int i = 4 * warp + 2 * (lane >> 4), j = (lane & 15) * 2;
         float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
-        const float* t0p = sT + (16 * a + r) * kStr + 16 * a;
-#pragma unroll 8
-        for (int l = 0; l < 16; ++l) {
-            const float t0v = t0p[l];
-            const float t1v = t0p[kStr + l];
-            const float2 xv = *reinterpret_cast<const float2*>(sX + b * 256 + l * 16 + c);
-            y00 = fmaf(t0v, xv.x, y00);
-            y01 = fmaf(t0v, xv.y, y01);
-            y10 = fmaf(t1v, xv.x, y10);
-            y11 = fmaf(t1v, xv.y, y11);
+        const float* t0p = sT + (32 + i) * kStr + 32;
+#pragma unroll 4
+        for (int c = 0; c < 4 * warp + 4; ++c) {
+            const float2 xv = *reinterpret_cast<const float2*>(sX + c * kXb + j);
+            const float t0 = t0p[c], t1 = t0p[kStr + c];
+            y00 = fmaf(t0, xv.x, y00);
+            y01 = fmaf(t0, xv.y, y01);
+            y10 = fmaf(t1, xv.x, y10);
+            y11 = fmaf(t1, xv.y, y11);
         }
-        *reinterpret_cast<float2*>(sT + (16 * a + r) * kStr + 16 * b + c) = make_float2(-y00, -y01);
-        *reinterpret_cast<float2*>(sT + (16 * a + r + 1) * kStr + 16 * b + c) =
-            make_float2(-y10, -y11);
+        *reinterpret_cast<float2*>(sT + (32 + i) * kStr + j) = make_float2(-y00, -y01);
+        *reinterpret_cast<float2*>(sT + (33 + i) * kStr + j) = make_float2(-y10, -y11);
     }
     sub_sync(bar_id);
 }
@@ -272,18 +309,22 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     const int half = tid >> 7;
     const int t0 = 32 * half;  // first token of this thread's half
 
-    // Issue the tile copies of one item's q, k, v, g (g on its own barrier, so
-    // the gate can start before q, k, v land) and set its beta.  Rows past the
-    // end of the tensor read as zeros; rows past the chunk's length (the next
-    // sequence's tokens) are zeroed after landing.
-    auto stage = [&](const ChunkInfo& c, int hh, float beta_t) {
+    // Issue the tile copies of one item's g (on its own barrier: the g tile's
+    // area is free once the previous item's score MMA has read it, so it is
+    // requested that early and the gate can start at once) and of its q, k, v
+    // (once the previous item's WY MMAs are done), and set its beta.  Rows past
+    // the end of the tensor read as zeros; rows past the chunk's length (the
+    // next sequence's tokens) are zeroed after landing.
+    auto stage_g = [&](int tok0, int hh) {  // thread 0
+        mbar_arrive_expect_tx(&S.bar_g, kChunk * kDim * 2);
+        tma_load_3d(sm + kSmG, &P.tm_g, 0, hh, tok0, &S.bar_g);
+    };
+    auto stage_qkv = [&](int tok0, int hh, float beta_t) {
         if (tid == 0) {
-            mbar_arrive_expect_tx(&S.bar_g, kChunk * kDim * 2);
-            tma_load_3d(sm + kSmG, &P.tm_g, 0, hh, c.tok0, &S.bar_g);
             mbar_arrive_expect_tx(&S.bar_qkv, 3 * kChunk * kDim * 2);
-            tma_load_3d(sm + kSmQ, &P.tm_q, 0, hh, c.tok0, &S.bar_qkv);
-            tma_load_3d(sm + kSmK, &P.tm_k, 0, hh, c.tok0, &S.bar_qkv);
-            tma_load_4d(sm + kSmV, &P.tm_v, 0, c.tok0, 0, hh, &S.bar_qkv);
+            tma_load_3d(sm + kSmQ, &P.tm_q, 0, hh, tok0, &S.bar_qkv);
+            tma_load_3d(sm + kSmK, &P.tm_k, 0, hh, tok0, &S.bar_qkv);
+            tma_load_4d(sm + kSmV, &P.tm_v, 0, tok0, 0, hh, &S.bar_qkv);
         }
         if (tid < kChunk) S.sBeta[tid] = beta_t;
     };
@@ -305,15 +346,18 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     int chunk = item / H;
     int h = item - chunk * H;
     ChunkInfo ci = P.info[chunk];
-    stage(ci, h, tid < kChunk ? load_beta(ci, h) : 0.f);
+    if (tid == 0) stage_g(ci.tok0, h);
+    stage_qkv(ci.tok0, h, tid < kChunk ? load_beta(ci, h) : 0.f);
     float dtb = P.dt_bias[h * kDim + ch];
     float alog = P.A_log[h];
     tc_fence_before();
     sub_sync(bar_id);
     tc_fence_after();
     const uint32_t tbase = S.tmem_base;
-    uint32_t tph = 0;       // phase of bar_g / bar_qkv for the current item
-    bool pending = true;    // an issued staging not yet waited for
+    // phases of bar_g / bar_qkv the next waits expect, and the copies issued and
+    // not yet waited for
+    uint32_t gph = 0, qph = 0;
+    bool g_out = true, qkv_out = true;
     int drain_mma = -1;     // after giving up on an MMA wait: the S.bar phase still owed
 
     for (;;) {
@@ -323,7 +367,12 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     const bool has_next = next < n_items;
     const int chunk_n = has_next ? next / H : chunk;
     const int h_n = has_next ? next - chunk_n * H : h;
-    if (!mbar_wait(&S.bar_g, tph, lim)) {
+    // first token of the next item, for its early g copy (thread 0)
+    const int tok0_n = (tid == 0 && has_next) ? P.info[chunk_n].tok0 : 0;
+    if (mbar_wait(&S.bar_g, gph, lim)) {
+        g_out = false;
+        gph ^= 1u;
+    } else {
         atomicOr(P.status, kStatusTimeout);
         S.s_abort = 1;
     }
@@ -353,13 +402,14 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         }
         S.sTot[half][ch] = prod;
     }
-    if (mbar_wait(&S.bar_qkv, tph, lim)) {
-        pending = false;
+    if (mbar_wait(&S.bar_qkv, qph, lim)) {
+        qkv_out = false;
+        qph ^= 1u;
     } else {
         atomicOr(P.status, kStatusTimeout);
         S.s_abort = 1;
     }
-    if (len < kChunk && !pending) {
+    if (len < kChunk && !qkv_out) {
         // zero the rows of tokens past the chunk's end in the q, k, v tiles
         for (int e = tid; e < 3 * kChunk * 16; e += kThreads) {
             const int tile = e / (kChunk * 16), r = (e / 16) % kChunk, piece = e & 15;
@@ -565,6 +615,11 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         drain_mma = 0;
         break;
     }
+    // the score MMA has read R, which covers the g tile: request the next item's g
+    if (has_next) {
+        if (tid == 0) stage_g(tok0_n, h_n);
+        g_out = true;
+    }
 
     // ---------------------------------------------------------------- score read-out
     // TMEM lane quarter w % 4 holds k rows (quarters 0, 1) or q rows (2, 3) of
@@ -678,10 +733,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         float* sT = reinterpret_cast<float*>(sm + kSmT);
         float* sX = reinterpret_cast<float*>(sm + kSmX);
         // (diagonal blocks: inverted above, after the score read-out)
-        // off-diagonal blocks, one diagonal distance d at a time
-        level_products<1>(sAT, sT, sX, tid, bar_id);
-        level_products<2>(sAT, sT, sX, tid, bar_id);
-        level_products<3>(sAT, sT, sX, tid, bar_id);
+        offdiag_inverse(sAT, sT, sX, tid, bar_id);
         // diag(beta) T^T as MN-major B operand: element (n = t, k = s) = beta_s T[t][s],
         // k-groups 128 B, n-groups 1024 B
 #pragma unroll
@@ -728,13 +780,12 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         break;
     }
 
-    // the staging area is free again: start the next item's copies
+    // the staging area of q, k, v is free again: start the next item's copies
     float beta_n = 0.f;
     if (has_next && tid < kChunk) beta_n = load_beta(ci_n, h_n);
     if (has_next) {
-        stage(ci_n, h_n, beta_n);
-        pending = true;
-        tph ^= 1u;
+        stage_qkv(ci_n.tok0, h_n, beta_n);
+        qkv_out = true;
     }
 
     // ---------------------------------------------------------------- W (warps 0-3), U^T (4-7)
@@ -778,10 +829,10 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     tc_fence_before();
     }  // item loop
 
-    if (pending && tid == 0) {
+    if (tid == 0) {
         // an aborted worker waits (bounded) for its own tile copies before leaving
-        mbar_drain(&S.bar_g, tph);
-        mbar_drain(&S.bar_qkv, tph);
+        if (g_out) mbar_drain(&S.bar_g, gph);
+        if (qkv_out) mbar_drain(&S.bar_qkv, qph);
     }
     // ... and for an MMA it stopped waiting for, before its TMEM is freed
     if (drain_mma >= 0 && tid == 0) mbar_drain(&S.bar, (uint32_t)drain_mma);

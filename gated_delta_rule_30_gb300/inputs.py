@@ -71,6 +71,9 @@ WORKLOADS["prefill_16k_16h"] = Workload("prefill_16k_16h: B=1 T=16384 H=16, fp32
 # smaller instance of long_context used for profiler captures (inputs still exceed L2)
 WORKLOADS["long_context_8k"] = Workload("long_context_8k: B=1 T=8192 H=32, fp32 state", 1, 8192,
                                         32, 3, state_dtype=torch.float32)
+# smaller decoding step used for profiler captures (states still exceed L2: 2 x 0.5 GB)
+WORKLOADS["decode_256"] = Workload("decode_256: B=256 T=1 H=32, fp32 state", 256, 1, 32, 5,
+                                   state_dtype=torch.float32)
 WORKLOAD_ORDER = ["ref_small", "dense_prefill", "varlen_packed", "long_context", "state_io"]
 
 

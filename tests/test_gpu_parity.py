@@ -99,7 +99,7 @@ def test_chunk_records_match_oracle_stages(kda_lib, oracle_mod):
                                    ("Aqk", d["Aqk"][:L, :L], scale * st["Aqk"])):
                 rel, mx = errors(gpu, ref)
                 print(f"\n[stage] {tag} {name}: rel_fro={rel:.3e} max_abs={mx:.3e}")
-                assert rel < 1e-2, f"{tag} {name}: rel_fro {rel:.3e}"
+                assert rel < 5e-3, f"{tag} {name}: rel_fro {rel:.3e}"
             np.testing.assert_allclose(d["gamma"], st["gamma"], rtol=1e-4, atol=1e-30,
                                        err_msg=tag)
             # padding rows/cols are exactly zero
