@@ -479,6 +479,8 @@ extern "C" kda_status_t kda_device_status(void* stream) {
     const int zero = 0;
     e = cudaMemcpyToSymbol(g_kda_status, &zero, sizeof(int));
     if (e != cudaSuccess) return cuda_error(e, "clear status");
+    if (host & kStatusLayout)
+        return set_error(KDA_ERR_CUDA, "a kernel's shared-memory area was not 1024-byte aligned");
     if (host & kStatusTimeout) return set_error(KDA_ERR_TIMEOUT, "a bounded device wait timed out");
     if (host & kStatusDeviceInput)
         return set_error(KDA_ERR_DEVICE_INPUT, "malformed cu_seqlens detected on the device");

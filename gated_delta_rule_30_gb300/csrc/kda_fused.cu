@@ -18,12 +18,14 @@
 #include "kda_prep.cuh"
 #include "kda_recur_t.cuh"
 
+
 namespace kda {
 namespace {
 
 constexpr int kFusedThreads = 2 * prep::kThreads;  // 512: two workers, or one recurrence
-constexpr uint32_t kFusedSmem = 2 * prep::kSmBytes > recur_t::kSmemBytes ? 2 * prep::kSmBytes
-                                                                          : recur_t::kSmemBytes;
+constexpr uint32_t kWorkerSmem = 2 * prep::kSmBytes;
+constexpr uint32_t kFusedSmem = kWorkerSmem > recur_t::kSmemBytes ? kWorkerSmem
+                                                                  : recur_t::kSmemBytes;
 static_assert(recur_t::kThreads <= kFusedThreads, "recurrence role needs more threads");
 static_assert(prep::kSmBytes % 1024 == 0, "worker areas must stay 1024-byte aligned");
 
@@ -34,6 +36,7 @@ struct FusedArgs {
     int n_rec;   // blocks running a recurrence (one per pair)
 };
 
+template <bool QKN>
 __global__ void __launch_bounds__(kFusedThreads, 1) fused_kernel(const __grid_constant__ FusedArgs A) {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ prep::PrepShared ps[2];
@@ -54,15 +57,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_kernel(const __grid_co
         __syncthreads();
         // both workers share the SM's TMEM (256 columns each); neither gives up
         // the allocation permit before the other has allocated.  Each worker's
-        // shared-memory area is a compile-time offset: with a run-time base the
-        // worker needs more registers and ran 5% slower.
+        // shared-memory area, barriers and role are compile-time constants, so
+        // the block holds two copies of the worker's code: one copy with
+        // run-time parameters needs more registers and ran 12% slower.
         // (named barriers: 1 and 2 span each worker, 3 and 4 its key-row warps)
         if ((int)threadIdx.x < prep::kThreads)
-            prep::prep_body(A.p, sm, ps[0], threadIdx.x, 1u, 3u, w0, workers, A.ready, false,
-                            &rdv, true, w0 + 1);
+            prep::prep_body<QKN>(A.p, sm, ps[0], threadIdx.x, 1u, 3u, w0, workers, A.ready,
+                                 false, &rdv, true, w0 + 1);
         else
-            prep::prep_body(A.p, sm + prep::kSmBytes, ps[1], threadIdx.x - prep::kThreads, 2u,
-                            4u, w0 + 1, workers, A.ready, false, &rdv, false, w0);
+            prep::prep_body<QKN>(A.p, sm + prep::kSmBytes, ps[1], threadIdx.x - prep::kThreads,
+                                 2u, 4u, w0 + 1, workers, A.ready, false, &rdv, false, w0);
     }
 }
 
@@ -79,14 +83,15 @@ bool fused_eligible(const Problem& p, bool forced) {
     if (forced ? pairs >= sms : 4 * pairs > sms) return false;
     // with few chunks per sequence there is little to overlap
     if (!forced && p.max_chunks < 8 * p.N) return false;
-    if (cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kFusedSmem) != cudaSuccess) {
+    const auto kern = p.qk_norm ? fused_kernel<true> : fused_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmem) !=
+        cudaSuccess) {
         cudaGetLastError();
         return false;
     }
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel, kFusedThreads,
-                                                      kFusedSmem) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFusedThreads, kFusedSmem) !=
+        cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -105,7 +110,8 @@ cudaError_t launch_fused(const Problem& p, const Workspace& ws, int* status, cud
     a.ready = ws.ready;
     a.n_rec = p.N * p.H;
     void* args[] = {&a};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fused_kernel), dim3(sms),
+    const auto kern = p.qk_norm ? fused_kernel<true> : fused_kernel<false>;
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(sms),
                                        dim3(kFusedThreads), args, kFusedSmem, st);
 }
 

@@ -57,9 +57,10 @@ namespace prep {
 constexpr int kThreads = 256;
 // shared memory map (bytes)
 constexpr uint32_t kSmQ = 0, kSmK = 16384, kSmG = 49152;  // staging tiles, row-major [64 t][128 c]
-// V^T as the A operand of U^T = V^T diag(beta) T^T, staged by TMA straight into the
-// MN-major core-matrix layout (8 value channels x 8 tokens per 128 B; token groups
-// 128 B apart, channel groups 1024 B apart): byte(v, t) = (v/8)*1024 + t*16 + (v%8)*2
+// V^T as the A operand of U^T = V^T diag(beta) T^T: the v tile lands row-major and
+// is moved in place (v_to_operand) into the MN-major core-matrix layout (8 value
+// channels x 8 tokens per 128 B; token groups 128 B apart, channel groups 1024 B
+// apart): byte(v, t) = (v/8)*1024 + t*16 + (v%8)*2
 constexpr uint32_t kSmV = 73728;      // 16 KB   (live until the WY MMAs)
 constexpr uint32_t kSmLeft = 0;       // 32 KB   (aliases the q, k tiles once they are consumed)
 constexpr uint32_t kSmR = 32768;      // 40 KB   R_0..R_3 (aliases the g tile)
@@ -78,11 +79,11 @@ __host__ __device__ constexpr uint32_t d_col(int a) { return 8u * a * (a + 1); }
 constexpr uint32_t kTmemCols = 256;
 
 struct PrepArgs {
-    // TMA descriptors of q, k, g viewed as [tokens][H][128] bf16 with a box of
-    // 64 tokens x 1 head x 128 channels (one 16 KB row-major tile per copy), and
-    // of v viewed as {8 channels, tokens, 16 channel groups, H} with a box of
-    // 8 x 64 x 16 x 1 (the MN-major operand layout of kSmV)
-    CUtensorMap tm_q, tm_k, tm_v, tm_g;
+    // TMA descriptors of q, k, v, g viewed as [tokens][H][128] bf16 with a box of
+    // 64 tokens x 1 head x 128 channels (one 16 KB row-major tile per copy); tm_ut: the U^T block
+    // of every record as [record][128 value channels][64 tokens] bf16 with a box of
+    // one record's block, 128-byte swizzled in shared memory (written by TMA store)
+    CUtensorMap tm_q, tm_k, tm_v, tm_g, tm_ut;
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;
@@ -117,44 +118,68 @@ __device__ __forceinline__ void stg_v4f(uint8_t* p, const float (&x)[8]) {
            pack_bf16(x[6], x[7]));
 }
 
-// Right factors of one sub-block pair owned by a half: for the local block
-// b0 (tokens 0..15 of the half, reference 7) and b1 (tokens 16..31,
-// reference 23), rf0[u] = exp(G_{7} - G_u) for u < 16 and rf1[u] =
-// exp(G_{23} - G_u) for u < 32 (local token indices).
-__device__ __forceinline__ void right_factors(const float (&al)[32], float (&rf0)[16],
-                                              float (&rf1)[32]) {
+// Factors of the right score operands, produced eight tokens at a time (the
+// arrays of a whole sub-block would hold up to 48 more registers at the phase
+// with the most live values).  For a reference token m of this half's tokens
+// (local indices), the factor of token u is exp(G_m - G_u):
+//   u <= m: prod_{s=u+1}^{m} alpha_s, a running product taken downwards from m;
+//   u >  m: 1 / prod_{s=m+1}^{u} alpha_s, taken as (prod_{s=u+1}^{e} alpha_s) /
+//           (prod_{s=m+1}^{e} alpha_s) over the tokens up to the group's end e.
+// back8(al, g, run, f): tokens 8g + 7 down to 8g of a downward run (run is the
+// product from the token above the group up to m; f[i] is token 8g + i).
+__device__ __forceinline__ void back8(const float (&al)[32], int g, float& run, float (&f)[8],
+                                      bool first) {
+    // (g is a compile-time constant at every call)
+#pragma unroll
+    for (int i = 7; i >= 0; --i) {
+        if (!(first && i == 7)) run *= al[8 * g + i + 1];
+        f[i] = run;
+    }
+}
+// fwd8(al, g, f): tokens 8g .. 8g + 7 after the reference 8g - 1:
+// f[i] = 1 / prod_{s=8g}^{8g+i} alpha_s.
+__device__ __forceinline__ void fwd8(const float (&al)[32], int g, float (&f)[8]) {
     float run = 1.f;
-    rf0[7] = 1.f;
 #pragma unroll
-    for (int u = 6; u >= 0; --u) {
-        run *= al[u + 1];
-        rf0[u] = run;
+    for (int i = 7; i >= 0; --i) {
+        f[i] = run;
+        run *= al[8 * g + i];
     }
-    run = 1.f;
+    const float inv = 1.f / run;
 #pragma unroll
-    for (int u = 15; u > 7; --u) {
-        rf0[u] = run;
-        run *= al[u];
+    for (int i = 0; i < 8; ++i) f[i] *= inv;
+}
+
+// The v tile lands row-major ([64 tokens][128 channels], 256-byte rows); the U
+// MMA reads it as the MN-major operand of kSmV.  The move permutes 16-byte
+// chunks (token t, channel group c8) -> (c8, t), in place, on 256 threads: every
+// thread first loads four chunks (v_tile_load), the caller synchronises, then
+// every thread writes them (v_tile_store).  A quarter-warp moves an 8 x 8 block
+// of chunks, lane i taking chunk (t0 + i, c0 + (i + s) % 8) at step s, so that
+// neither the reads (rows 256 B apart) nor the writes (groups 1024 B apart) meet
+// a bank conflict.  Tokens t >= len are written as zeros.
+__device__ __forceinline__ void v_chunk(int tid, int j, int& t, int& c8) {
+    const int qw = tid >> 3, i = tid & 7;
+    const int blk = qw >> 1, s = 4 * (qw & 1) + j;
+    t = 8 * (blk & 7) + i;
+    c8 = 8 * (blk >> 3) + ((i + s) & 7);
+}
+__device__ __forceinline__ void v_tile_load(const uint8_t* tile, int tid, int len, uint4 (&x)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        int t, c8;
+        v_chunk(tid, j, t, c8);
+        x[j] = t < len ? *reinterpret_cast<const uint4*>(tile + t * 256 + c8 * 16)
+                       : make_uint4(0u, 0u, 0u, 0u);
     }
-    float inv = 1.f / run;
+}
+__device__ __forceinline__ void v_tile_store(uint8_t* tile, int tid, const uint4 (&x)[4]) {
 #pragma unroll
-    for (int u = 8; u < 16; ++u) rf0[u] *= inv;
-    run = 1.f;
-    rf1[23] = 1.f;
-#pragma unroll
-    for (int u = 22; u >= 0; --u) {
-        run *= al[u + 1];
-        rf1[u] = run;
+    for (int j = 0; j < 4; ++j) {
+        int t, c8;
+        v_chunk(tid, j, t, c8);
+        *reinterpret_cast<uint4*>(tile + c8 * 1024 + t * 16) = x[j];
     }
-    run = 1.f;
-#pragma unroll
-    for (int u = 31; u > 23; --u) {
-        rf1[u] = run;
-        run *= al[u];
-    }
-    inv = 1.f / run;
-#pragma unroll
-    for (int u = 24; u < 32; ++u) rf1[u] *= inv;
 }
 
 // Per-worker state that lives outside the dynamic shared-memory area.
@@ -168,14 +193,15 @@ struct PrepShared {
     uint64_t bar_qkv;   // q, k, v tiles landed
     uint32_t tmem_base;
     int s_abort;
+    int pending;  // with `ready`: the item whose flag waits for its U^T store (thread 0)
 };
 
 // Barrier over the kThreads threads of one worker.
 __device__ __forceinline__ void sub_sync(uint32_t bar_id) {
     asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kThreads) : "memory");
 }
-// One TMA tile copy (box of the tensor map at coordinates {x, y, z} / {x, y, z, w})
-// into shared memory, completing on `bar`.
+// One TMA tile copy (box of the tensor map at coordinates {x, y, z}) into shared
+// memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
                                             uint64_t* bar) {
     asm volatile(
@@ -184,13 +210,29 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
         : "memory");
 }
-__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z,
-                                            int w, uint64_t* bar) {
+// TMA tensor store of one box from shared memory, in the thread's bulk async-group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z,
+                                             const void* src) {
     asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-        "%3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar))
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
         : "memory");
+}
+// Row `ch` (64 bf16 values, 128 B) of a 128 x 64 tile in the 128-byte swizzled
+// layout the tensor store reads: 16-byte chunk j of row ch sits in slot
+// j ^ (ch % 8), so the eight rows a quarter-warp writes fall in distinct banks.
+// r[c][u] holds the value of column 16 c + u.
+__device__ __forceinline__ void sts_row_swizzled(uint8_t* tile, int ch, const uint32_t (&r)[4][16]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t* x = &r[j >> 1][8 * (j & 1)];
+        st_shared_v4(smem_addr(tile + ch * 128 + ((j ^ (ch & 7)) << 4)),
+                     pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                     pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                     pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                     pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
+    }
 }
 __device__ __forceinline__ void st_release_gpu(int* p, int v) {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -299,6 +341,11 @@ __device__ __forceinline__ void offdiag_inverse(const float* sAT, float* sT, flo
 // times, so neither waits for a meeting the other never reaches, and worker 0's
 // meeting in item k depends only on its own item k, worker 1's only on finishing
 // item k - 1; the wait is bounded like every other.
+//
+// QKN: normalise the q and k rows first (P.qk_norm); a template parameter so
+// that the common kernels carry none of that code (the worker's instruction
+// footprint matters when two copies share an SM).
+template <bool QKN>
 __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepShared& S,
                                           const int tid, const uint32_t bar_id,
                                           const uint32_t bar_k, const int first_item,
@@ -310,7 +357,14 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     if (P.flags[0] != 1) return;
     // a CTA that already gave up on a bounded wait poisons the launch: skip the
     // rest (decided once, so every thread of the worker takes the same path)
-    if (tid == 0) S.s_abort = (*((volatile int*)P.status) & kStatusTimeout) ? 1 : 0;
+    if (tid == 0) {
+        S.s_abort = (*((volatile int*)P.status) & kStatusTimeout) ? 1 : 0;
+        // the swizzled U^T staging tile needs a 1024-byte aligned area
+        if (smem_addr(sm) & 1023u) {
+            atomicOr(P.status, kStatusLayout);
+            S.s_abort = 1;
+        }
+    }
     sub_sync(bar_id);
     if (S.s_abort) return;
     const uint64_t lim = wait_limit_ns(P.status);  // of every wait that may give up
@@ -338,7 +392,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
             mbar_arrive_expect_tx(&S.bar_qkv, 3 * kChunk * kDim * 2);
             tma_load_3d(sm + kSmQ, &P.tm_q, 0, hh, tok0, &S.bar_qkv);
             tma_load_3d(sm + kSmK, &P.tm_k, 0, hh, tok0, &S.bar_qkv);
-            tma_load_4d(sm + kSmV, &P.tm_v, 0, tok0, 0, hh, &S.bar_qkv);
+            tma_load_3d(sm + kSmV, &P.tm_v, 0, hh, tok0, &S.bar_qkv);
         }
         if (tid < kChunk) S.sBeta[tid] = beta_t;
     };
@@ -356,6 +410,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         mbar_init(&S.bar_qkv, 1);
         mbar_fence_init();
         S.s_abort = 0;
+        S.pending = -1;
     }
     int chunk = item / H;
     int h = item - chunk * H;
@@ -444,20 +499,34 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         S.s_abort = 1;
     }
     if (len < kChunk && !qkv_out) {
-        // zero the rows of tokens past the chunk's end in the q, k, v tiles
-        for (int e = tid; e < 3 * kChunk * 16; e += kThreads) {
+        // zero the rows of tokens past the chunk's end in the q, k tiles (the v tile's
+        // are zeroed when it is moved into the operand layout)
+        for (int e = tid; e < 2 * kChunk * 16; e += kThreads) {
             const int tile = e / (kChunk * 16), r = (e / 16) % kChunk, piece = e & 15;
-            if (r >= len) {
-                uint8_t* p = tile < 2 ? sm + tile * 16384 + r * 256 + piece * 16
-                                      : sm + kSmV + piece * 1024 + r * 16;  // channel group `piece`
-                *reinterpret_cast<uint4*>(p) = make_uint4(0u, 0u, 0u, 0u);
+            if (r >= len)
+                *reinterpret_cast<uint4*>(sm + tile * 16384 + r * 256 + piece * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    if (tid == 0) {
+        // the previous item's U^T tensor store has read the (K o E)^T area; with
+        // `ready`, it has completed, and the previous item's flag is published
+        // (here, a gate phase after the store was issued, rather than at once)
+        if (ready) {
+            bulk_wait<0>();
+            if (S.pending >= 0) {
+                fence_async_global();
+                st_release_gpu(ready + S.pending, 1);
+                S.pending = -1;
             }
+        } else {
+            bulk_wait_read<0>();
         }
     }
     sub_sync(bar_id);           // q, k, v, S.sTot, S.sQf visible
     if (S.s_abort) break;
     uint32_t qp[16], kp[16];
-    if (P.qk_norm) {
+    if (QKN) {
         // 1 / sqrt(|x|^2 + eps) of each q row (r < 64) and k row (r >= 64), two
         // threads per row; zeroed padding rows stay zero
         {
@@ -542,30 +611,28 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         for (int bl = 0; bl < 2; ++bl) {
             const int a = 2 * half + bl;  // global sub-block
             const int u0 = 16 * bl;       // its first local token
-            float lf[16];
-            float run = 1.f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                run *= al[u0 + u];
-                lf[u] = run;
-            }
-            const float inv = 1.f / lf[7];
-#pragma unroll
-            for (int u = 0; u < 7; ++u) lf[u] *= inv;
-            lf[7] = 1.f;
-            run = 1.f;
-#pragma unroll
-            for (int u = 8; u < 16; ++u) {
-                run *= al[u0 + u];
-                lf[u] = run;
-            }
+            // (eight tokens at a time: tokens u0 .. u0 + 7 relative to the reference
+            // u0 + 7, then u0 + 8 .. u0 + 15)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
+                float lf[8];
+                float run = 1.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    run *= al[u0 + hh * 8 + u];
+                    lf[u] = run;
+                }
+                if (hh == 0) {
+                    const float inv = 1.f / lf[7];
+#pragma unroll
+                    for (int u = 0; u < 7; ++u) lf[u] *= inv;
+                    lf[7] = 1.f;
+                }
                 float kl[8], ql[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    kl[u] = KV(u0 + hh * 8 + u) * lf[hh * 8 + u];
-                    ql[u] = QV(u0 + hh * 8 + u) * lf[hh * 8 + u];
+                    kl[u] = KV(u0 + hh * 8 + u) * lf[u];
+                    ql[u] = QV(u0 + hh * 8 + u) * lf[u];
                 }
                 sts_v4f(smem_addr(sm + kSmLeft + mnmaj_off(16 * a + 8 * hh, ch, 128, 2048)), kl);
                 sts_v4f(smem_addr(sm + kSmLeft + mnmaj_off(64 + 16 * a + 8 * hh, ch, 128, 2048)),
@@ -574,43 +641,48 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         }
         // right operands inside this half: R_{2h} rows [32h, 32h+16), R_{2h+1} rows [32h, 32h+32)
         {
-            float rf0[16], rf1[32];
-            right_factors(al, rf0, rf1);
+            // R_{2h}: reference local token 7 (groups 0 down, then group 1 up);
+            // R_{2h+1}: reference 23 (groups 2, 1, 0 down, then group 3 up)
             const int a0 = 2 * half, a1 = 2 * half + 1;
-#pragma unroll
-            for (int jg = 0; jg < 2; ++jg) {
+            auto put = [&](int a, int g, const float (&f)[8]) {
                 float r8[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) r8[u] = KV(jg * 8 + u) * rf0[jg * 8 + u];
-                sts_v4f(smem_addr(sm + kSmR + r_off(a0) + mnmaj_off(t0 + jg * 8, ch, 128, 2048)),
-                        r8);
-            }
-#pragma unroll
-            for (int jg = 0; jg < 4; ++jg) {
-                float r8[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) r8[u] = KV(jg * 8 + u) * rf1[jg * 8 + u];
-                sts_v4f(smem_addr(sm + kSmR + r_off(a1) + mnmaj_off(t0 + jg * 8, ch, 128, 2048)),
-                        r8);
-            }
+                for (int u = 0; u < 8; ++u) r8[u] = KV(g * 8 + u) * f[u];
+                sts_v4f(smem_addr(sm + kSmR + r_off(a) + mnmaj_off(t0 + g * 8, ch, 128, 2048)), r8);
+            };
+            float f[8];
+            float run = 1.f;
+            back8(al, 0, run, f, true);
+            put(a0, 0, f);
+            fwd8(al, 1, f);
+            put(a0, 1, f);
+            run = 1.f;
+            back8(al, 2, run, f, true);
+            put(a1, 2, f);
+            back8(al, 1, run, f, false);
+            put(a1, 1, f);
+            back8(al, 0, run, f, false);
+            put(a1, 0, f);
+            fwd8(al, 3, f);
+            put(a1, 3, f);
         }
         if (half == 0) {
             // R_2 and R_3 rows [0, 32): prod_{j+1}^{31} alpha (local) times the
             // second half's prod_{32}^{m_a} alpha
             const float q2 = S.sQf[0][ch], q3 = S.sQf[1][ch];
             float run = 1.f;
-            float sfx[32];
 #pragma unroll
-            for (int u = 31; u >= 0; --u) {
-                sfx[u] = run;
-                run *= al[u];
-            }
+            for (int jg = 3; jg >= 0; --jg) {  // prod_{s=u+1}^{31} alpha_s, downwards
+                float sfx[8];
 #pragma unroll
-            for (int jg = 0; jg < 4; ++jg) {
+                for (int u = 7; u >= 0; --u) {
+                    sfx[u] = run;
+                    run *= al[jg * 8 + u];
+                }
                 float r2[8], r3[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const float kv = KV(jg * 8 + u) * sfx[jg * 8 + u];
+                    const float kv = KV(jg * 8 + u) * sfx[u];
                     r2[u] = kv * q2;
                     r3[u] = kv * q3;
                 }
@@ -769,6 +841,13 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         float* sX = reinterpret_cast<float*>(sm + kSmX);
         // (diagonal blocks: inverted above, after the score read-out)
         offdiag_inverse(sAT, sT, sX, tid, bar_id);
+        // the v tile into the operand layout (its copy landed with q and k)
+        {
+            uint4 vx[4];
+            v_tile_load(sm + kSmV, tid, len, vx);
+            sub_sync(bar_id);
+            v_tile_store(sm + kSmV, tid, vx);
+        }
         // diag(beta) T^T as MN-major B operand: element (n = t, k = s) = beta_s T[t][s],
         // k-groups 128 B, n-groups 1024 B
 #pragma unroll
@@ -824,6 +903,10 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     }
 
     // ---------------------------------------------------------------- W (warps 0-3), U^T (4-7)
+    // W goes to the record with coalesced stores; U^T (one 128-byte record row per
+    // value channel) is staged in the (K o E)^T area, which the W MMA has finished
+    // reading, and written by one TMA store; the next item's prefix pass, the
+    // area's next writer, starts after thread 0 has seen the store read it.
     {
         const bool is_w = warp < 4;
         const uint32_t col0 = is_w ? 0u : 64u;
@@ -833,26 +916,30 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence16(r[c]);
+        if (is_w) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 4; ++c) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float x[8];
+                for (int hh = 0; hh < 2; ++hh) {
+                    float x[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) x[u] = __uint_as_float(r[c][8 * hh + u]);
-                if (is_w)
+                    for (int u = 0; u < 8; ++u) x[u] = __uint_as_float(r[c][8 * hh + u]);
                     stg_v4f(rec + kRecWQ + mnmaj_off(16 * c + 8 * hh, ch, 128, 2048), x);
-                else
-                    stg_v4f(rec + kRecUT + ch * 128 + (16 * c + 8 * hh) * 2, x);
+                }
             }
+        } else {
+            sts_row_swizzled(sm + kSmKbT, ch, r);
+            fence_async_smem();
         }
     }
-
-    if (ready) {
-        // the barrier orders every thread's record stores before thread 0's
-        // release, which publishes them at GPU scope with the flag
-        sub_sync(bar_id);
-        if (tid == 0) st_release_gpu(ready + item, 1);
+    // the barrier orders every thread's record stores and U^T staging before thread 0's
+    // tensor store and flag release
+    sub_sync(bar_id);
+    if (tid == 0) {
+        tma_store_3d(&P.tm_ut, 0, 0, chunk * H + h, sm + kSmKbT);
+        bulk_commit();
+        // the flag follows once the store has completed (next item, or the exit)
+        if (ready) S.pending = item;
     }
     ++it;
     if (!has_next) break;
@@ -866,6 +953,12 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     }  // item loop
 
     if (tid == 0) {
+        // the last U^T store, then the last flag
+        bulk_wait<0>();
+        if (ready && S.pending >= 0) {
+            fence_async_global();
+            st_release_gpu(ready + S.pending, 1);
+        }
         // an aborted worker waits (bounded) for its own tile copies before leaving
         if (g_out) mbar_drain(&S.bar_g, gph);
         if (qkv_out) mbar_drain(&S.bar_qkv, qph);
@@ -908,19 +1001,18 @@ inline bool encode_tile_map(CUtensorMap* m, const void* base, int64_t tokens, in
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [tokens][H][128] bf16 viewed as {8 channels, tokens, 16 channel groups, H}
-// -> boxes of 8 x 64 x 16 x 1 that land as [group][token][8 channels], the
-// MN-major core-matrix layout of a 128-channel x 64-token operand (channel
-// groups 1024 B apart, token groups 128 B apart).
-inline bool encode_operand_map(CUtensorMap* m, const void* base, int64_t tokens, int H) {
+// The U^T block of every record: {64 tokens, 128 value channels, n_rec records},
+// rows 128 B apart, records kRecBytes apart -> boxes of one record's 64 x 128,
+// 128-byte swizzled in shared memory.
+inline bool encode_ut_map(CUtensorMap* m, uint8_t* records, int64_t n_rec) {
     const EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return false;
-    const cuuint64_t dims[4] = {8u, (cuuint64_t)tokens, (cuuint64_t)(kDim / 8), (cuuint64_t)H};
-    const cuuint64_t strides[3] = {(cuuint64_t)H * kDim * 2, 16u, (cuuint64_t)kDim * 2};  // bytes
-    const cuuint32_t box[4] = {8u, (cuuint32_t)kChunk, (cuuint32_t)(kDim / 8), 1u};
-    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    const cuuint64_t dims[3] = {(cuuint64_t)kChunk, (cuuint64_t)kDim, (cuuint64_t)n_rec};
+    const cuuint64_t strides[2] = {(cuuint64_t)kChunk * 2, (cuuint64_t)kRecBytes};  // bytes
+    const cuuint32_t box[3] = {(cuuint32_t)kChunk, (cuuint32_t)kDim, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, records + kRecUT, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -945,8 +1037,9 @@ inline bool make_prep_args(const Problem& p, const Workspace& ws, int* status, P
     a.status = status;
     return encode_tile_map(&a.tm_q, p.q, p.total_tokens, p.H) &&
            encode_tile_map(&a.tm_k, p.k, p.total_tokens, p.H) &&
-           encode_operand_map(&a.tm_v, p.v, p.total_tokens, p.H) &&
-           encode_tile_map(&a.tm_g, p.g, p.total_tokens, p.H);
+           encode_tile_map(&a.tm_v, p.v, p.total_tokens, p.H) &&
+           encode_tile_map(&a.tm_g, p.g, p.total_tokens, p.H) &&
+           encode_ut_map(&a.tm_ut, ws.records, (int64_t)p.max_chunks * p.H);
 }
 
 }  // namespace prep

@@ -120,11 +120,6 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-// Order this thread's generic-proxy view of global memory (made visible by an
-// acquire) before its later async-proxy (bulk copy) reads.
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
 // Wait (bounded by `limit` ns) until *flag is non-zero.
 __device__ __forceinline__ bool wait_flag(const int* flag, uint64_t limit) {
     if (ld_acquire_gpu(flag) != 0) return true;
@@ -383,7 +378,8 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
                             S.s_abort = 1;
                             break;
                         }
-                        fence_proxy_async_global();
+                        // the acquired view of the record before the bulk copy's reads
+                        fence_async_global();
                     }
                     mbar_arrive_expect_tx(&S.full[s], kRecBytes);
                     bulk_g2s(sm + s * kStageBytes,

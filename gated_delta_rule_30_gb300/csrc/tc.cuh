@@ -135,7 +135,23 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
+// bulk async-groups of the calling thread (bulk and tensor stores to global memory)
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most N of the thread's groups are still reading their shared-memory source
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// wait until at most N of the thread's groups are still incomplete (writes not yet performed)
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
 // ----------------------------------------------------------------------------- fences
+// order async-proxy (bulk copy) global accesses with the thread's generic-proxy ones
+__device__ __forceinline__ void fence_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -263,14 +279,19 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 
 // ----------------------------------------------------------------------------- transcendentals
 // Hardware base-2 exponential / logarithm (PTX ex2.approx / lg2.approx).
+// The hardware base-2 exponential and logarithm (one MUFU operation each), with
+// subnormal inputs and results flushed to zero.  Their one user, the chunk
+// kernel's gate, never depends on a subnormal: the logarithm's inputs lie in
+// (1, 2], 2^-|x| is subnormal only where 1 + 2^-|x| already rounds to 1, and the
+// decays are at least e^-10 (the library rejects lower_bound < -10).
 __device__ __forceinline__ float hw_exp2(float x) {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 __device__ __forceinline__ float hw_log2(float x) {
     float y;
-    asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 

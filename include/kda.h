@@ -180,8 +180,10 @@ size_t kda_noalloc_scratch_bytes(void);
 /*
  * kda_device_status -- synchronises `stream`, then returns and clears the
  * library's per-device status word: KDA_OK, KDA_ERR_DEVICE_INPUT (malformed
- * cu_seqlens seen by an earlier call) or KDA_ERR_TIMEOUT (a bounded
- * device-side wait gave up; that call's outputs are undefined).
+ * cu_seqlens seen by an earlier call), KDA_ERR_TIMEOUT (a bounded
+ * device-side wait gave up; that call's outputs are undefined) or KDA_ERR_CUDA
+ * (a chunk kernel found its shared-memory area misaligned for its swizzled
+ * tensor store and skipped its work; outputs undefined).
  */
 kda_status_t kda_device_status(void* stream);
 
