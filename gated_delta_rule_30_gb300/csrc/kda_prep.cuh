@@ -77,6 +77,14 @@ __host__ __device__ constexpr uint32_t r_off(int a) { return 2048u * a * (a + 1)
 // score block a occupies TMEM columns [8 a (a+1), 8 (a+1)(a+2)): 0, 16, 48, 96
 __host__ __device__ constexpr uint32_t d_col(int a) { return 8u * a * (a + 1); }
 constexpr uint32_t kTmemCols = 256;
+// The thread that issues the U^T tensor stores and, in the fused launch,
+// publishes the ready flags: lane 0 of warp 2, a q-row warp of the score
+// read-out, which has slack there while warps 0 and 1 invert the diagonal
+// blocks (the bulk-group waits must come from the issuing thread; thread 0 is on
+// every critical path, and a GPU-scope release taken there stalled its whole
+// worker: fused launch 1.40 -> 1.23 ms with the workers alone).
+constexpr int kStoreTid = 64;
+
 
 struct PrepArgs {
     // TMA descriptors of q, k, v, g viewed as [tokens][H][128] bf16 with a box of
@@ -193,7 +201,7 @@ struct PrepShared {
     uint64_t bar_qkv;   // q, k, v tiles landed
     uint32_t tmem_base;
     int s_abort;
-    int pending;  // with `ready`: the item whose flag waits for its U^T store (thread 0)
+    int pending;  // with `ready`: the item whose flag waits for its U^T store (kStoreTid)
 };
 
 // Barrier over the kThreads threads of one worker.
@@ -234,8 +242,19 @@ __device__ __forceinline__ void sts_row_swizzled(uint8_t* tile, int ch, const ui
                      pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
     }
 }
-__device__ __forceinline__ void st_release_gpu(int* p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_relaxed_gpu(int* p, int v) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Publish ready[item] = 1 once every store of that record is performed: the
+// calling thread's tensor stores (waited for), then, through a GPU-scope fence,
+// everything ordered before this thread.  (The fence costs about a thousand
+// cycles of the SM's progress, wherever it is taken; batching several flags
+// behind one fence did not shorten the fused launch.)
+__device__ __forceinline__ void publish_flag(int* ready, int item) {
+    bulk_wait<0>();
+    fence_async_global();
+    __threadfence();
+    st_relaxed_gpu(ready + item, 1);
 }
 
 // Off-diagonal part of T = (I + A)^-1 from its four diagonal 16 x 16 blocks
@@ -508,21 +527,9 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
                     make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    if (tid == 0) {
-        // the previous item's U^T tensor store has read the (K o E)^T area; with
-        // `ready`, it has completed, and the previous item's flag is published
-        // (here, a gate phase after the store was issued, rather than at once)
-        if (ready) {
-            bulk_wait<0>();
-            if (S.pending >= 0) {
-                fence_async_global();
-                st_release_gpu(ready + S.pending, 1);
-                S.pending = -1;
-            }
-        } else {
-            bulk_wait_read<0>();
-        }
-    }
+    // the previous item's U^T tensor store has read the (K o E)^T area, which the
+    // prefix pass below rewrites
+    if (tid == kStoreTid) bulk_wait_read<0>();
     sub_sync(bar_id);           // q, k, v, S.sTot, S.sQf visible
     if (S.s_abort) break;
     uint32_t qp[16], kp[16];
@@ -796,6 +803,13 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
                 const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
                 sT[(16 * a + r) * kStr + 16 * b + c] = 0.f;
             }
+            if (ready && tid == kStoreTid && S.pending >= 0) {
+                // the previous item's U^T store has completed (a gate phase and more
+                // ago): publish its record (every other store of it is ordered before
+                // by the barriers since)
+                publish_flag(ready, S.pending);
+                S.pending = -1;
+            }
         } else {
             // A^T is complete once the four k-row warps have stored it; warps 0 and 1
             // then invert the four 16 x 16 diagonal blocks of I + A by forward
@@ -932,13 +946,14 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
             fence_async_smem();
         }
     }
-    // the barrier orders every thread's record stores and U^T staging before thread 0's
-    // tensor store and flag release
+    // the barrier orders every thread's record stores and U^T staging before the
+    // tensor store and the flag release
     sub_sync(bar_id);
-    if (tid == 0) {
+    if (tid == kStoreTid) {
         tma_store_3d(&P.tm_ut, 0, 0, chunk * H + h, sm + kSmKbT);
         bulk_commit();
-        // the flag follows once the store has completed (next item, or the exit)
+        // the flag follows once the store has completed (next item's read-out, or
+        // the exit)
         if (ready) S.pending = item;
     }
     ++it;
@@ -952,13 +967,12 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     tc_fence_before();
     }  // item loop
 
-    if (tid == 0) {
+    if (tid == kStoreTid) {
         // the last U^T store, then the last flag
         bulk_wait<0>();
-        if (ready && S.pending >= 0) {
-            fence_async_global();
-            st_release_gpu(ready + S.pending, 1);
-        }
+        if (ready && S.pending >= 0) publish_flag(ready, S.pending);
+    }
+    if (tid == 0) {
         // an aborted worker waits (bounded) for its own tile copies before leaving
         if (g_out) mbar_drain(&S.bar_g, gph);
         if (qkv_out) mbar_drain(&S.bar_qkv, qph);

@@ -133,16 +133,32 @@ __device__ __forceinline__ bool wait_flag(const int* flag, uint64_t limit) {
     }
 }
 
+// Each record reaches its ring slot in two parts.  Part A (W and scale*Q o E,
+// U^T, exp(G_last)) is what a chunk needs first, and its readers are done once
+// the chunk's Delta is computed; part B ((K o F)^T and scale*Aqk) is needed only
+// for the state update and the outputs.  So part A of chunk i + 2 is copied as
+// soon as chunk i has computed Delta, over a chunk ahead of its use, and part B
+// once chunk i's MMAs are done: a record copy no longer has to fit in one
+// chunk's processing time (with the fused launch's memory traffic it did not).
+constexpr uint32_t kPartA0 = kRecWQ, kPartA0Bytes = kRecKT - kRecWQ;        // W, Q
+constexpr uint32_t kPartA1 = kRecUT, kPartA1Bytes = kRecBytes - kRecUT;     // U^T, gamma
+constexpr uint32_t kPartB = kRecKT, kPartBBytes = kRecUT - kRecKT;          // K^T, Aqk hi/lo
+static_assert(kPartA0Bytes + kPartA1Bytes + kPartBBytes == kRecBytes, "record parts");
+static_assert(kRecWQ == 0 && kRecKT < kRecAQ && kRecAQ < kRecAQL && kRecAQL < kRecUT &&
+                  kRecUT < kRecGam,
+              "part A = [0, KT) + [UT, end), part B = [KT, UT)");
+
 // Small per-block state that lives outside the dynamic shared-memory area.
-// full/empty: record ring; s_ready[r]: round r of the snapshot written (key
+// full/fullB: parts A/B of a record landed; emptyA: part A of the slot read
+// (Delta computed); empty: the slot's MMAs done; s_ready[r]: round r of the snapshot written (key
 // channels 64 h + 32 r .. + 31 of both halves h); mma1: X^T ready;
 // d_ready: Delta^T written; mma2s: state updated; mma2o[b]: outputs of the
 // chunk in X[b] complete; x_free[b]: the output warps have read X[b];
 // tile_full[b]: output tile b is written; mma_done: every MMA the block
 // issued has completed (waited for once, before TMEM is freed)
 struct RecurTShared {
-    uint64_t full[kStages], empty[kStages], s_ready[2], mma1, d_ready, mma2s, mma2o[2], x_free[2],
-        tile_full[2], mma_done;
+    uint64_t full[kStages], fullB[kStages], emptyA[kStages], empty[kStages], s_ready[2], mma1,
+        d_ready, mma2s, mma2o[2], x_free[2], tile_full[2], mma_done;
     uint32_t tmem_base;
     int s_abort;
 };
@@ -209,6 +225,8 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&S.full[s], 1);
+            mbar_init(&S.fullB[s], 1);
+            mbar_init(&S.emptyA[s], 32 * kEpiWarps);
             mbar_init(&S.empty[s], 1);
         }
         mbar_init(&S.s_ready[0], 32 * kEpiWarps);
@@ -325,6 +343,9 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&S.d_ready);
+                // gamma and U^T are read and MMA1 (the reader of W, Q) has completed:
+                // part A of the slot may take chunk i + 2's
+                mbar_arrive(&S.emptyA[s]);
             }
             WAIT_OR_ABORT(&S.mma2s, ph);
             tc_fence_after();
@@ -357,7 +378,7 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
         if (warp == kWarpProducer) {
             // ---------------------------------------------------- producer
             if (lane == 0) {
-                int fills[kStages] = {0, 0};
+                int fillsA[kStages] = {0, 0}, fillsB[kStages] = {0, 0};
                 constexpr int kAhead = kStages + 2;  // records pulled into L2 ahead
                 if (!ready)
                     for (int i = 0; i < kAhead && i < nchunks; ++i)
@@ -365,7 +386,10 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
                                          kRecBytes);
                 for (int i = 0; i < nchunks; ++i) {
                     const int s = i % kStages;
-                    if (fills[s] > 0) WAIT_OR_ABORT(&S.empty[s], (uint32_t)((fills[s] - 1) & 1));
+                    uint8_t* dst = sm + s * kStageBytes;
+                    const uint8_t* rec = P.records + ((size_t)(c_begin + i) * H + h) * kRecBytes;
+                    // part A once the chunk last in this slot has computed its Delta
+                    if (fillsA[s] > 0) WAIT_OR_ABORT(&S.emptyA[s], (uint32_t)((fillsA[s] - 1) & 1));
                     if (*((volatile int*)&S.s_abort)) break;
                     if (!ready && i + kAhead < nchunks)
                         bulk_prefetch_l2(
@@ -381,16 +405,24 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
                         // the acquired view of the record before the bulk copy's reads
                         fence_async_global();
                     }
-                    mbar_arrive_expect_tx(&S.full[s], kRecBytes);
-                    bulk_g2s(sm + s * kStageBytes,
-                             P.records + ((size_t)(c_begin + i) * H + h) * kRecBytes, kRecBytes,
-                             &S.full[s]);
-                    ++fills[s];
+                    mbar_arrive_expect_tx(&S.full[s], kPartA0Bytes + kPartA1Bytes);
+                    bulk_g2s(dst + kPartA0, rec + kPartA0, kPartA0Bytes, &S.full[s]);
+                    bulk_g2s(dst + kPartA1, rec + kPartA1, kPartA1Bytes, &S.full[s]);
+                    ++fillsA[s];
+                    // part B once that chunk's MMAs are done
+                    if (fillsB[s] > 0) WAIT_OR_ABORT(&S.empty[s], (uint32_t)((fillsB[s] - 1) & 1));
+                    if (*((volatile int*)&S.s_abort)) break;
+                    mbar_arrive_expect_tx(&S.fullB[s], kPartBBytes);
+                    bulk_g2s(dst + kPartB, rec + kPartB, kPartBBytes, &S.fullB[s]);
+                    ++fillsB[s];
                 }
                 // drain: every issued fill must have landed before the CTA exits
-                for (int s = 0; s < kStages; ++s)
-                    if (fills[s] > 0 && !mbar_drain(&S.full[s], (uint32_t)((fills[s] - 1) & 1)))
+                for (int s = 0; s < kStages; ++s) {
+                    if (fillsA[s] > 0 && !mbar_drain(&S.full[s], (uint32_t)((fillsA[s] - 1) & 1)))
                         atomicOr(P.status, kStatusTimeout);
+                    if (fillsB[s] > 0 && !mbar_drain(&S.fullB[s], (uint32_t)((fillsB[s] - 1) & 1)))
+                        atomicOr(P.status, kStatusTimeout);
+                }
             }
         } else if (warp == kWarpMma) {
             // ---------------------------------------------------- MMA issuer
@@ -438,6 +470,7 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
                 }
                 __syncwarp();
                 WAIT_OR_ABORT(&S.d_ready, ph);
+                WAIT_OR_ABORT(&S.fullB[s], (uint32_t)((i / kStages) & 1));
                 tc_fence_after();
                 if (elect_one()) {
 #pragma unroll
