@@ -48,13 +48,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_kernel(const __grid_co
     } else {
         const int workers = 2 * ((int)gridDim.x - A.n_rec);
         const int w0 = 2 * ((int)blockIdx.x - A.n_rec);
-        // the two workers' per-item meeting point (see prep_body)
-        __shared__ uint64_t rdv;
-        if (threadIdx.x == 0) {
-            mbar_init(&rdv, 2);
-            mbar_fence_init();
-        }
-        __syncthreads();
         // both workers share the SM's TMEM (256 columns each); neither gives up
         // the allocation permit before the other has allocated.  Each worker's
         // shared-memory area, barriers and role are compile-time constants, so
@@ -63,10 +56,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_kernel(const __grid_co
         // (named barriers: 1 and 2 span each worker, 3 and 4 its key-row warps)
         if ((int)threadIdx.x < prep::kThreads)
             prep::prep_body<QKN>(A.p, sm, ps[0], threadIdx.x, 1u, 3u, w0, workers, A.ready,
-                                 false, &rdv, true, w0 + 1);
+                                 false);
         else
             prep::prep_body<QKN>(A.p, sm + prep::kSmBytes, ps[1], threadIdx.x - prep::kThreads,
-                                 2u, 4u, w0 + 1, workers, A.ready, false, &rdv, false, w0);
+                                 2u, 4u, w0 + 1, workers, A.ready, false);
     }
 }
 

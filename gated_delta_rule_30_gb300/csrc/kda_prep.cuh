@@ -349,18 +349,6 @@ __device__ __forceinline__ void offdiag_inverse(const float* sAT, float* sT, flo
 // publishes ready[item] = 1 (release, GPU scope) once an item's record is
 // complete.
 //
-// With `rdv` non-null (two workers in one block) the worker meets its partner
-// (first item `partner_first`) once per item on the mbarrier `rdv` (count 2):
-// worker 0 after issuing its score MMA, worker 1 at the start of its item
-// (`rdv_at_mma` selects the point).  This keeps one worker in its elementwise
-// phases (gate, operands) while the other runs its latency-bound ones (MMA
-// waits, the inverse), instead of both drifting into the same phase (fused
-// launch on long_context: 1.90 -> 1.85 ms; meeting after worker 0's read-out or
-// inverse instead measured 1.90 ms).  They meet min(own, partner's) item count
-// times, so neither waits for a meeting the other never reaches, and worker 0's
-// meeting in item k depends only on its own item k, worker 1's only on finishing
-// item k - 1; the wait is bounded like every other.
-//
 // QKN: normalise the q and k rows first (P.qk_norm); a template parameter so
 // that the common kernels carry none of that code (the worker's instruction
 // footprint matters when two copies share an SM).
@@ -369,9 +357,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
                                           const int tid, const uint32_t bar_id,
                                           const uint32_t bar_k, const int first_item,
                                           const int item_stride, int* ready,
-                                          const bool relinquish, uint64_t* rdv = nullptr,
-                                          const bool rdv_at_mma = false,
-                                          const int partner_first = 0) {
+                                          const bool relinquish) {
 
     if (P.flags[0] != 1) return;
     // a CTA that already gave up on a bounded wait poisons the launch: skip the
@@ -447,25 +433,6 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     uint32_t gph = 0, qph = 0;
     bool g_out = true, qkv_out = true;
     int drain_mma = -1;     // after giving up on an MMA wait: the S.bar phase still owed
-    // meetings with the partner worker: one per item, min of both item counts
-    int meetings = 0;
-    if (rdv) {
-        const int n_mine = (n_items - first_item + item_stride - 1) / item_stride;
-        const int n_part = partner_first < n_items
-                               ? (n_items - partner_first + item_stride - 1) / item_stride
-                               : 0;
-        meetings = n_mine < n_part ? n_mine : n_part;
-    }
-    int it = 0;  // items done
-    auto meet = [&]() {  // thread 0
-        if (it < meetings) {
-            mbar_arrive(rdv);
-            if (!mbar_wait(rdv, (uint32_t)(it & 1), lim)) {
-                atomicOr(P.status, kStatusTimeout);
-                S.s_abort = 1;
-            }
-        }
-    };
 
     for (;;) {
     const int len = ci.len;
@@ -476,7 +443,6 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     const int h_n = has_next ? next - chunk_n * H : h;
     // first token of the next item, for its early g copy (thread 0)
     const int tok0_n = (tid == 0 && has_next) ? P.info[chunk_n].tok0 : 0;
-    if (rdv && !rdv_at_mma && tid == 0) meet();
     if (mbar_wait(&S.bar_g, gph, lim)) {
         g_out = false;
         gph ^= 1u;
@@ -717,7 +683,6 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         for (int kk = 0; kk < 8; ++kk)
             mma_bf16(tbase, dl + 16u * kk, dr + 16u * kk, idesc, kk > 0 ? 1u : 0u);
         mma_commit(&S.bar);
-        if (rdv && rdv_at_mma) meet();
     }
     if (!mbar_wait(&S.bar, 0, lim)) {
         atomicOr(P.status, kStatusTimeout);
@@ -956,7 +921,6 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
         // the exit)
         if (ready) S.pending = item;
     }
-    ++it;
     if (!has_next) break;
     item = next;
     chunk = chunk_n;
