@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) Kimi Delta Attention forward pass.
+"""GB300 (sm_103a) Kimi Delta Attention forward pass (and its backward pass).
 
 Thin Python binding over the C ABI in ``include/kda.h`` (``libkda.so``, built
 in-tree by ``gated_delta_rule_30_gb300.build``).  This module only marshals
@@ -12,13 +12,15 @@ Kernel API":
 
     fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
         initial_state=None, final_state=None, cu_seqlens=None)
+
+``bwd`` returns the gradients of that operation (``kda_bwd``).
 """
 from __future__ import annotations
 
 import ctypes
 import os
 
-__all__ = ["fwd", "chunk_kda", "lib", "library_path", "workspace_size", "device_status",
+__all__ = ["fwd", "chunk_kda", "bwd", "bwd_workspace_size", "lib", "library_path", "workspace_size", "device_status",
            "KDAError",
            "selftest_tcgen05", "set_recurrence_kernel", "set_stage_events", "last_path",
            "set_wait_limit_ns"]
@@ -81,6 +83,11 @@ def lib():
         L.kda_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         L.kda_set_wait_limit_ns.restype = ctypes.c_int
         L.kda_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        L.kda_bwd.restype = ctypes.c_int
+        L.kda_bwd.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, f32, vp, ctypes.c_int, vp, vp, vp,
+                              i32, i32, i32, i32, i32, i32] + [vp] * 8 + [vp, ctypes.c_size_t, vp]
+        L.kda_bwd_workspace_size.restype = ctypes.c_size_t
+        L.kda_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         L.kda_selftest_tcgen05.restype = ctypes.c_int
         L.kda_selftest_tcgen05.argtypes = [vp, vp, vp, i32, i32, vp]
         _lib = L
@@ -229,6 +236,92 @@ def chunk_kda(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale=None, initial
     fwd(q, k, v, g, beta, scale, o, A_log, dt_bias, lower_bound, initial_state=initial_state,
         final_state=hT, cu_seqlens=cu_seqlens, use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel)
     return o, hT
+
+
+def bwd_workspace_size(B: int, T: int, H: int, num_seqs: int = 0,
+                       has_cu_seqlens: bool = False) -> int:
+    n = lib().kda_bwd_workspace_size(B, T, H, num_seqs, 1 if has_cu_seqlens else 0)
+    if n == 0:
+        _check(1)
+    return int(n)
+
+
+def bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_state=None,
+        dfinal_state=None, cu_seqlens=None, workspace=None, want_dh0=True):
+    """Backward pass of ``fwd`` on the GPU (``kda_bwd``): gradients of
+    L = sum(dout * out) + sum(dfinal_state * final_state).
+
+    Inputs as for ``fwd``; ``dout``: bf16, shaped like ``v``; ``dfinal_state``:
+    fp32 [N, H, 128, 128] or None.  Returns a dict of new fp32 tensors: dq, dk,
+    dg (like q), dv (like v), dbeta (like beta), dA_log [H], ddt_bias [H, 128]
+    and dh0 [N, H, 128, 128] (None when ``want_dh0`` is false).  ``workspace``:
+    optional uint8 device tensor of at least ``bwd_workspace_size`` bytes; by
+    default the per-(device, stream) buffer that ``fwd`` also uses is grown and
+    reused.
+    """
+    import torch
+    L = lib()
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("dout", dout)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, K]")
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if k.shape != q.shape or g.shape != q.shape:
+        raise ValueError("k and g must have q's shape")
+    if tuple(v.shape) != (B, T, H, V) or tuple(dout.shape) != (B, T, H, V):
+        raise ValueError("v and dout must be [B, T, H, V]")
+    if tuple(beta.shape) != (B, T, H):
+        raise ValueError("beta must be [B, T, H]")
+    for name, t, shp in (("A_log", A_log, (H,)), ("dt_bias", dt_bias, (H, K))):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 \
+                or not t.is_contiguous() or tuple(t.shape) != shp:
+            raise ValueError(f"{name} must be a contiguous CUDA float32 tensor of shape {shp}")
+    num_seqs = 0
+    if cu_seqlens is not None:
+        if not cu_seqlens.is_cuda or cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 \
+                or not cu_seqlens.is_contiguous():
+            raise ValueError("cu_seqlens must be a contiguous 1-D int32 CUDA tensor")
+        num_seqs = cu_seqlens.numel() - 1
+    N = num_seqs if cu_seqlens is not None else B
+    if initial_state is not None:
+        if not initial_state.is_cuda or not initial_state.is_contiguous() \
+                or tuple(initial_state.shape) != (N, H, K, V):
+            raise ValueError(f"initial_state must be a contiguous CUDA tensor of shape {(N, H, K, V)}")
+    if dfinal_state is not None:
+        if not dfinal_state.is_cuda or not dfinal_state.is_contiguous() \
+                or dfinal_state.dtype != torch.float32 or tuple(dfinal_state.shape) != (N, H, K, V):
+            raise ValueError("dfinal_state must be a contiguous CUDA float32 tensor of shape "
+                             f"{(N, H, K, V)}")
+    dev = q.device
+    f32 = torch.float32
+    res = {"dq": torch.empty(q.shape, dtype=f32, device=dev),
+           "dk": torch.empty(q.shape, dtype=f32, device=dev),
+           "dv": torch.empty(v.shape, dtype=f32, device=dev),
+           "dg": torch.empty(q.shape, dtype=f32, device=dev),
+           "dbeta": torch.empty(beta.shape, dtype=f32, device=dev),
+           "dA_log": torch.empty((H,), dtype=f32, device=dev),
+           "ddt_bias": torch.empty((H, K), dtype=f32, device=dev),
+           "dh0": torch.empty((N, H, K, V), dtype=f32, device=dev) if want_dh0 else None}
+    stream = _stream_ptr(dev)
+    with torch.cuda.device(dev):
+        need = L.kda_bwd_workspace_size(B, T, H, num_seqs, 1 if cu_seqlens is not None else 0)
+        if need == 0:
+            _check(1)
+        ws = workspace if workspace is not None else _workspace(dev, stream, need)
+        _check(L.kda_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(A_log),
+                         _ptr(dt_bias), float(lower_bound), _ptr(initial_state),
+                         _state_dtype(initial_state), _ptr(dout), _ptr(dfinal_state),
+                         _ptr(cu_seqlens), int(num_seqs), B, T, H, K, V,
+                         *(_ptr(res[n]) for n in ("dq", "dk", "dv", "dg", "dbeta", "dA_log",
+                                                  "ddt_bias", "dh0")),
+                         ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(ws.numel()), stream))
+    return res
 
 
 def fwd_alloc(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,

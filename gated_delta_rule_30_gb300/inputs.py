@@ -18,6 +18,10 @@ with ``seed``, in this order:
 
 ``lower_bound = -5`` and ``scale = K ** -0.5`` unless overridden.
 
+``cotangents`` draws the backward pass's output gradients from a second
+generator seeded with ``seed + 1000``: ``dout = randn`` shaped like ``v``
+(bf16), then ``dfinal_state = randn(N, H, K, V)`` (fp32).
+
 The five named workloads are those the benchmark and the parity tests use;
 ``shrink`` gives a smaller instance of the same recipe for fast tests.
 """
@@ -128,6 +132,15 @@ def make(w: Workload, K: int = K_DIM, V: int = V_DIM) -> dict:
                 lower_bound=float(w.lower_bound), scale=1.0 / math.sqrt(K),
                 initial_state=h0, state_dtype=w.state_dtype, cu_seqlens=cu, B=B, T=T, H=H, N=N,
                 K=K, V=V, name=w.name)
+
+
+def cotangents(p: dict, seed: int) -> dict:
+    """Seeded gradients of the forward's outputs for a problem drawn by ``make``
+    (see module docstring); ``seed`` is the workload's seed."""
+    gen = torch.Generator(device="cpu").manual_seed(seed + 1000)
+    dout = torch.randn(tuple(p["v"].shape), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    dfinal = torch.randn((p["N"], p["H"], p["K"], p["V"]), generator=gen, dtype=torch.float32)
+    return dict(dout=dout, dfinal_state=dfinal)
 
 
 def head_tokens(p: dict) -> int:

@@ -178,6 +178,52 @@ kda_status_t kda_fwd_noalloc(const void* q, const void* k, const void* v, const 
 size_t kda_noalloc_scratch_bytes(void);
 
 /*
+ * kda_bwd -- backward pass of kda_fwd (no counterpart on the pages, which
+ * print the forward call only; the operation differentiated is the one stated
+ * at the top of this file, q and k used as given).  Computes the gradients of
+ *     L = sum(dout * out) + sum(dfinal_state * final_state)
+ * with respect to every input:
+ *   dq, dk, dg     fp32 [B, T, H, K], written
+ *   dv             fp32 [B, T, H, V], written
+ *   dbeta          fp32 [B, T, H], written
+ *   dA_log         fp32 [H], written (sum over all sequences and tokens)
+ *   ddt_bias       fp32 [H, K], written (likewise)
+ *   dinitial_state fp32 [N, H, K, V], written, or NULL (not wanted)
+ * Inputs are those of kda_fwd (same layouts, dtypes and constraints on q, k,
+ * v, g, beta, A_log, dt_bias, initial_state, cu_seqlens and the sizes) plus
+ *   dout           bf16 [B, T, H, V], the gradient of out
+ *   dfinal_state   fp32 [N, H, K, V], or NULL (no final-state term)
+ * lower_bound: finite, <= 0 (no other range limit: the backward pass does not
+ * use the forward's sub-block factorisation).  The clamp max(pre, lower_bound)
+ * passes its gradient to the argument it returns, and to pre at a tie.
+ * Arithmetic is fp32 throughout, token by token; the results are
+ * deterministic (every sum is taken in a fixed order).
+ * All pointers are DEVICE memory owned by the caller, 16-byte aligned (beta:
+ * 2-byte, dbeta: 4-byte); outputs must not overlap inputs or one another.
+ * `workspace`: device memory of at least kda_bwd_workspace_size(...) bytes,
+ * 256-byte aligned, or NULL to take it from the stream-ordered allocator on
+ * `stream` (workspace_bytes is then ignored).  The scratch holds an fp32 copy
+ * of the state entering every 16-token segment: about 4 KB per token per head.
+ * Asynchronous on `stream`; argument errors are reported synchronously and
+ * launch nothing.  A malformed cu_seqlens (as for kda_fwd) is detected on the
+ * device: the affected sequences are skipped and kda_device_status reports
+ * KDA_ERR_DEVICE_INPUT; the gradients of that call are then undefined.
+ */
+kda_status_t kda_bwd(const void* q, const void* k, const void* v, const void* g,
+                     const void* beta, float scale, const float* A_log, const float* dt_bias,
+                     float lower_bound, const void* initial_state, kda_dtype_t initial_dtype,
+                     const void* dout, const float* dfinal_state, const int32_t* cu_seqlens,
+                     int32_t num_seqs, int32_t B, int32_t T, int32_t H, int32_t K, int32_t V,
+                     float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dA_log,
+                     float* ddt_bias, float* dinitial_state, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/* Bytes of device scratch kda_bwd needs for these sizes (does not read
+ * cu_seqlens).  Returns 0 and sets the error message for invalid sizes. */
+size_t kda_bwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t num_seqs,
+                              int32_t has_cu_seqlens);
+
+/*
  * kda_device_status -- synchronises `stream`, then returns and clears the
  * library's per-device status word: KDA_OK, KDA_ERR_DEVICE_INPUT (malformed
  * cu_seqlens seen by an earlier call), KDA_ERR_TIMEOUT (a bounded

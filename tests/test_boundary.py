@@ -178,3 +178,44 @@ def test_workspace_size_single_token_step(kda_lib):
         assert L.kda_workspace_size(1024, 1, 32, 0, 0) > 64 << 20
     finally:
         kda_lib.set_recurrence_kernel("auto")
+
+
+def call_bwd(kda_lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=0.088, A_log=FAKE, dt_bias=FAKE,
+             lb=-5.0, h0=None, h0d=0, dout=FAKE, dhT=None, cu=None, ns=0, B=1, T=64, H=2, K=128,
+             V=128, dq=FAKE, dk=FAKE, dv=FAKE, dg=FAKE, dbeta=FAKE, dA=FAKE, ddt=FAKE, dh0=None,
+             ws=FAKE, wsb=0)
+    a.update(over)
+    L = kda_lib.lib()
+    rc = L.kda_bwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["A_log"],
+                   a["dt_bias"], a["lb"], a["h0"], a["h0d"], a["dout"], a["dhT"], a["cu"], a["ns"],
+                   a["B"], a["T"], a["H"], a["K"], a["V"], a["dq"], a["dk"], a["dv"], a["dg"],
+                   a["dbeta"], a["dA"], a["ddt"], a["dh0"], a["ws"], a["wsb"], None)
+    return rc, L.kda_last_error_message().decode()
+
+
+@pytest.mark.parametrize("over", [
+    dict(K=64), dict(V=64), dict(H=0), dict(T=-1), dict(B=0), dict(B=2, cu=FAKE, ns=2),
+    dict(h0=FAKE, h0d=3), dict(h0=FAKE, h0d=0), dict(h0=None, h0d=2),
+    dict(lb=0.5), dict(lb=float("nan")), dict(scale=float("nan")),
+    dict(dout=None), dict(dq=None), dict(dA=None), dict(ddt=None), dict(A_log=None),
+    dict(dout=FAKE + 8), dict(dv=FAKE + 4), dict(dbeta=FAKE + 2), dict(dhT=FAKE + 8),
+    dict(dh0=FAKE + 8), dict(cu=FAKE + 2, ns=1), dict(cu=FAKE, ns=-1),
+    dict(wsb=1),                      # caller workspace smaller than kda_bwd_workspace_size
+])
+def test_bwd_invalid_arguments_rejected(kda_lib, over):
+    rc, msg = call_bwd(kda_lib, **over)
+    assert rc == 1, (rc, msg)
+    assert msg
+
+
+def test_bwd_workspace_size(kda_lib):
+    """Per-pair partial sums plus one fp32 state slice set (128 x 128) per head for
+    each of floor(total / 16) + N + 1 checkpoint slots."""
+    L = kda_lib.lib()
+    n = L.kda_bwd_workspace_size(8, 2048, 16, 0, 0)
+    slots = 8 * 2048 // 16 + 8 + 1
+    ckpt = slots * 16 * 128 * 128 * 4
+    assert ckpt <= n <= ckpt + 8 * 16 * (4 + 128) * 4 + 512
+    assert L.kda_bwd_workspace_size(2, 64, 1, 3, 1) == 0
+    assert L.kda_bwd_workspace_size(1, 100, 2, 3, 1) > 0
