@@ -64,7 +64,8 @@ constexpr int kSmSt = 0;                                         // float4 [kHal
 constexpr int kSmQ = kSmSt + kHalf * 4 * kThreads * 16;          // float [kSeg][128]
 constexpr int kSmK = kSmQ + kSeg * kDim * 4;                     // float [kSeg][128]
 constexpr int kSmA = kSmK + kSeg * kDim * 4;                     // float [kSeg][128] decays
-constexpr int kSmV = kSmA + kSeg * kDim * 4;                     // float [kSeg][kVs]
+constexpr int kSmX = kSmA + kSeg * kDim * 4;                     // float [kSeg][128] g + dt_bias
+constexpr int kSmV = kSmX + kSeg * kDim * 4;                     // float [kSeg][kVs]
 constexpr int kSmDO = kSmV + kSeg * kVs * 4;                     // float [kSeg][kVs]
 constexpr int kSmB = kSmDO + kSeg * kVs * 4;                     // float [kSeg]
 constexpr int kSmSlot = kSmB + kSeg * 4;                         // float [2][kWarps][kPart]
@@ -121,14 +122,28 @@ __device__ __forceinline__ void gate(float x, float expA, float lb, float& pre, 
     a = expf(fmaxf(pre, lb));
 }
 
-// Column sums over the 32 lanes of a warp (all lanes end with the same sums:
-// each butterfly step adds the same two values on both partners).
+// Column sums over the 32 lanes of a warp, every lane ending with the same
+// sums.  Reduce-scatter, then gather: lanes exchange half of their partial
+// sums with the lane 16 apart (each keeping two columns), then half again with
+// the lane 8 apart (one column), sum that column over the 8 lanes that share
+// it by a butterfly (each step adds the same two values on both partners, so
+// the 8 lanes agree), and finally read the other columns' sums from lanes of
+// the groups that hold them: 10 shuffles instead of 20 for a plain butterfly.
 __device__ __forceinline__ void warp_sum4(float (&p)[4]) {
+    const int lane = threadIdx.x & 31;
+    const bool hi4 = lane & 16, hi3 = lane & 8;
+    float q0 = hi4 ? p[2] : p[0], q1 = hi4 ? p[3] : p[1];
+    q0 += __shfl_xor_sync(0xffffffffu, hi4 ? p[0] : p[2], 16);
+    q1 += __shfl_xor_sync(0xffffffffu, hi4 ? p[1] : p[3], 16);
+    // q0, q1: columns 2 hi4 + 0, 2 hi4 + 1
+    float w = hi3 ? q1 : q0;
+    w += __shfl_xor_sync(0xffffffffu, hi3 ? q0 : q1, 8);
+    // w: column 2 hi4 + hi3
+    w += __shfl_xor_sync(0xffffffffu, w, 4);
+    w += __shfl_xor_sync(0xffffffffu, w, 2);
+    w += __shfl_xor_sync(0xffffffffu, w, 1);
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-#pragma unroll
-        for (int m = 0; m < 4; ++m) p[m] += __shfl_xor_sync(0xffffffffu, p[m], o);
-    }
+    for (int m = 0; m < 4; ++m) p[m] = __shfl_sync(0xffffffffu, w, (m >> 1) * 16 + (m & 1) * 8 + (lane & 7));
 }
 
 __device__ __forceinline__ void ld4(const float* p, float (&x)[4]) {
@@ -162,77 +177,121 @@ __device__ __forceinline__ void fwd_token(float (&S)[4][4], const float (&a)[4],
         for (int m = 0; m < 4; ++m) S[i][m] = fmaf(kk[i], u[m], S[i][m]);
 }
 
-// Stages one segment's token data in shared memory as fp32: q, k and the
-// decays a of all 128 key channels, v and dout of this CTA's value columns,
-// beta.  Rows at or past len are zero (never used).  with_q: also q and dout.
-__device__ __forceinline__ void stage_segment(const BwdArgs& P, uint8_t* sm, long long row0,
-                                              int h, int len, int col0, float expA,
-                                              bool with_q, int tid) {
-    float* qs = reinterpret_cast<float*>(sm + kSmQ);
-    float* ks = reinterpret_cast<float*>(sm + kSmK);
-    float* as = reinterpret_cast<float*>(sm + kSmA);
-    float* vs = reinterpret_cast<float*>(sm + kSmV);
-    float* dos = reinterpret_cast<float*>(sm + kSmDO);
-    float* bs = reinterpret_cast<float*>(sm + kSmB);
-    const int H = P.H;
-    {   // 16 tokens x 128 channels = 256 pieces of 8 channels, one per thread
-        const int t = tid >> 4, c8 = (tid & 15) * 8;
-        float kq[8], qq[8], aa[8];
-        if (t < len) {
-            const long long off = ((row0 + t) * H + h) * kDim + c8;
-            const uint4 kr = *reinterpret_cast<const uint4*>(P.k + off);
-            const uint4 gr = *reinterpret_cast<const uint4*>(P.g + off);
-            const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kr);
-            const __nv_bfloat16* gb = reinterpret_cast<const __nv_bfloat16*>(&gr);
-            const float* dtb = P.dt_bias + (long long)h * kDim + c8;
+// Column sums of eight values per lane (see warp_sum4): reduce-scatter over
+// the lane bits 4, 3 and 2 (four, two and one shuffles), a butterfly over the
+// four lanes that share a value, then the gather: 17 shuffles instead of 40.
+__device__ __forceinline__ void warp_sum8(float (&p)[8]) {
+    const int lane = threadIdx.x & 31;
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    // value index bits: bit 2 <- lane bit 4, bit 1 <- lane bit 3, bit 0 <- lane bit 2
+    float q[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                kq[e] = __bfloat162float(kb[e]);
-                float pre;
-                gate(__bfloat162float(gb[e]) + dtb[e], expA, P.lower_bound, pre, aa[e]);
-            }
-            if (with_q) {
-                const uint4 qr = *reinterpret_cast<const uint4*>(P.q + off);
-                const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&qr);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) qq[e] = __bfloat162float(qb[e]);
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) kq[e] = qq[e] = aa[e] = 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; e += 4) {
-            *reinterpret_cast<float4*>(ks + t * kDim + c8 + e) =
-                make_float4(kq[e], kq[e + 1], kq[e + 2], kq[e + 3]);
-            *reinterpret_cast<float4*>(as + t * kDim + c8 + e) =
-                make_float4(aa[e], aa[e + 1], aa[e + 2], aa[e + 3]);
-            if (with_q)
-                *reinterpret_cast<float4*>(qs + t * kDim + c8 + e) =
-                    make_float4(qq[e], qq[e + 1], qq[e + 2], qq[e + 3]);
-        }
+    for (int j = 0; j < 4; ++j) {
+        const float keep = b4 ? p[4 + j] : p[j], send = b4 ? p[j] : p[4 + j];
+        q[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
     }
-    // v and dout: 16 tokens x 32 columns = 64 pieces of 8 each
-    if (tid < 128 && (tid < 64 || with_q)) {
-        const int piece = tid & 63, t = piece >> 2, c8 = (piece & 3) * 8;
-        const __nv_bfloat16* src = tid < 64 ? P.v : P.dout;
-        float* dst = tid < 64 ? vs : dos;
-        float x[8];
-        if (t < len) {
-            const uint4 r = *reinterpret_cast<const uint4*>(src + ((row0 + t) * H + h) * kDim +
-                                                           col0 + c8);
-            const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(&r);
+    float r[2];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = __bfloat162float(rb[e]);
-        } else {
+    for (int j = 0; j < 2; ++j) {
+        const float keep = b3 ? q[2 + j] : q[j], send = b3 ? q[j] : q[2 + j];
+        r[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float w = b2 ? r[1] : r[0];
+    w += __shfl_xor_sync(0xffffffffu, b2 ? r[0] : r[1], 4);
+    w += __shfl_xor_sync(0xffffffffu, w, 2);
+    w += __shfl_xor_sync(0xffffffffu, w, 1);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+    for (int m = 0; m < 8; ++m) p[m] = __shfl_sync(0xffffffffu, w, m * 4 + (lane & 3));
+}
+
+// Split cluster barrier: arrive (releasing this thread's shared-memory writes
+// to the other CTAs of the cluster), then later wait (acquiring theirs).
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// One segment's token data as loaded from global memory (bf16 bit patterns),
+// held in registers so that the loads of the next segment overlap the work on
+// the current one.  Thread t: channels 8 (t % 16) .. + 7 of token t / 16 of k,
+// g and q; threads 0..63 eight values of v, threads 64..127 of dout (this
+// CTA's value columns); threads 128..143 the beta of one token.  Zero past len.
+struct Fetched {
+    uint4 k, g, q, vd;
+    float beta;
+};
+
+__device__ __forceinline__ void fetch_segment(const BwdArgs& P, long long row0, int h, int len,
+                                              int col0, bool with_q, int tid, Fetched& F) {
+    const int H = P.H;
+    const int t = tid >> 4, c8 = (tid & 15) * 8;
+    F.k = F.g = F.q = F.vd = make_uint4(0u, 0u, 0u, 0u);
+    F.beta = 0.f;
+    if (t < len) {
+        const long long off = ((row0 + t) * H + h) * kDim + c8;
+        F.k = *reinterpret_cast<const uint4*>(P.k + off);
+        F.g = *reinterpret_cast<const uint4*>(P.g + off);
+        if (with_q) F.q = *reinterpret_cast<const uint4*>(P.q + off);
+    }
+    if (tid < 128) {
+        const int piece = tid & 63, tv = piece >> 2, cv = (piece & 3) * 8;
+        if (tv < len && (tid < 64 || with_q)) {
+            const __nv_bfloat16* src = tid < 64 ? P.v : P.dout;
+            F.vd = *reinterpret_cast<const uint4*>(src + ((row0 + tv) * H + h) * kDim + col0 + cv);
         }
-        *reinterpret_cast<float4*>(dst + t * kVs + c8) = make_float4(x[0], x[1], x[2], x[3]);
-        *reinterpret_cast<float4*>(dst + t * kVs + c8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
-    } else if (tid >= 128 && tid < 128 + kSeg) {
-        const int t = tid - 128;
-        bs[t] = t < len ? __bfloat162float(P.beta[(row0 + t) * H + h]) : 0.f;
+    } else if (tid < 128 + kSeg && tid - 128 < len) {
+        F.beta = __bfloat162float(P.beta[(row0 + (tid - 128)) * H + h]);
+    }
+}
+
+// Writes fetched token data to shared memory as fp32: k, q, the gate argument
+// x = g + dt_bias and the decay a of all 128 key channels, v and dout of this
+// CTA's columns, beta.  dtb: dt_bias of the thread's eight channels.
+// with_q: also q and dout.
+__device__ __forceinline__ void store_segment(uint8_t* sm, const Fetched& F, const float (&dtb)[8],
+                                              float expA, float lb, bool with_q, int tid) {
+    const int t = tid >> 4, c8 = (tid & 15) * 8;
+    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&F.k);
+    const __nv_bfloat16* gb = reinterpret_cast<const __nv_bfloat16*>(&F.g);
+    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&F.q);
+    float kk[8], xx[8], aa[8], qq[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        kk[e] = __bfloat162float(kb[e]);
+        qq[e] = __bfloat162float(qb[e]);
+        xx[e] = __bfloat162float(gb[e]) + dtb[e];
+        float pre;
+        gate(xx[e], expA, lb, pre, aa[e]);
+    }
+    const int base = t * kDim + c8;
+#pragma unroll
+    for (int e = 0; e < 8; e += 4) {
+        *reinterpret_cast<float4*>(sm + kSmK + 4 * (base + e)) =
+            make_float4(kk[e], kk[e + 1], kk[e + 2], kk[e + 3]);
+        *reinterpret_cast<float4*>(sm + kSmA + 4 * (base + e)) =
+            make_float4(aa[e], aa[e + 1], aa[e + 2], aa[e + 3]);
+        *reinterpret_cast<float4*>(sm + kSmX + 4 * (base + e)) =
+            make_float4(xx[e], xx[e + 1], xx[e + 2], xx[e + 3]);
+        if (with_q)
+            *reinterpret_cast<float4*>(sm + kSmQ + 4 * (base + e)) =
+                make_float4(qq[e], qq[e + 1], qq[e + 2], qq[e + 3]);
+    }
+    if (tid < 128) {
+        if (tid < 64 || with_q) {
+            const int piece = tid & 63, tv = piece >> 2, cv = (piece & 3) * 8;
+            const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(&F.vd);
+            float* dst = reinterpret_cast<float*>(sm + (tid < 64 ? kSmV : kSmDO)) + tv * kVs + cv;
+            *reinterpret_cast<float4*>(dst) =
+                make_float4(__bfloat162float(vb[0]), __bfloat162float(vb[1]),
+                            __bfloat162float(vb[2]), __bfloat162float(vb[3]));
+            *reinterpret_cast<float4*>(dst + 4) =
+                make_float4(__bfloat162float(vb[4]), __bfloat162float(vb[5]),
+                            __bfloat162float(vb[6]), __bfloat162float(vb[7]));
+        }
+    } else if (tid < 128 + kSeg) {
+        reinterpret_cast<float*>(sm + kSmB)[tid - 128] = F.beta;
     }
 }
 
@@ -282,9 +341,13 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
         L = P.T;
     }
     const float expA = expf(P.A_log[h]);
+    float dtb[8];  // dt_bias of the eight channels this thread stages
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dtb[e] = P.dt_bias[(long long)h * kDim + (tid & 15) * 8 + e];
     const float* qs = reinterpret_cast<const float*>(sm + kSmQ);
     const float* ks = reinterpret_cast<const float*>(sm + kSmK);
     const float* as = reinterpret_cast<const float*>(sm + kSmA);
+    const float* xs = reinterpret_cast<const float*>(sm + kSmX);
     const float* vs = reinterpret_cast<const float*>(sm + kSmV);
     const float* dos = reinterpret_cast<const float*>(sm + kSmDO);
     const float* bs = reinterpret_cast<const float*>(sm + kSmB);
@@ -322,14 +385,19 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
         return reinterpret_cast<float4*>(P.ckpt + (((slot0 + s) * H + h) * kSlices + rank) *
                                                       (long long)kSliceElems);
     };
+    Fetched F;
 
     // 1. forward sweep: the state entering every segment (the last segment's
-    //    tokens are replayed by the walk, so the sweep stops before them)
+    //    tokens are replayed by the walk, so the sweep stops before them);
+    //    the next segment's loads are in flight while a segment is swept
+    if (nseg > 1) fetch_segment(P, row0, h, kSeg, col0, false, tid, F);
     for (int s = 0; s < nseg; ++s) {
         save_piece(ckpt_at(s), S, tid);  // read back later by this same thread
         if (s == nseg - 1) break;
         __syncthreads();
-        stage_segment(P, sm, row0 + (long long)s * kSeg, h, kSeg, col0, expA, false, tid);
+        store_segment(sm, F, dtb, expA, lb, false, tid);
+        if (s + 2 < nseg)
+            fetch_segment(P, row0 + (long long)(s + 1) * kSeg, h, kSeg, col0, false, tid, F);
         __syncthreads();
         for (int t = 0; t < kSeg; ++t) {
             float a[4], kk[4], vv[4];
@@ -340,20 +408,69 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
         }
     }
 
-    // 2. backward walk, segments last to first, each in two halves
+    // 2. backward walk, segments last to first, each in two halves.  The row
+    //    sums of a half are taken over the cluster after the next half's
+    //    states are recomputed, which hides the cluster barrier's latency.
     float accA = 0.f, accB = 0.f;  // dA_log and ddt_bias of key channel 32 rank + lane
     int cb = 0;                    // part[] buffer of the current half
+    bool pend = false;             // a walked half whose row sums are not yet taken
+    long long p_row = 0;           // its first token's row
+    int p_len = 0, p_cb = 0;
+    float p_x = 0.f;               // gate argument of (its token warp, channel 32 rank + lane)
+    auto finish_half = [&]() {
+        cluster_wait();
+        if (warp < p_len) {
+            const int c = rank * kVs + lane;
+            const long long row = p_row + warp;
+            float sq = 0.f, sk = 0.f, sa = 0.f, sb = 0.f;
+#pragma unroll
+            for (int r = 0; r < kSlices; ++r) {
+                const float* rp =
+                    cluster.map_shared_rank(part + (p_cb * kHalf + warp) * kPart, (unsigned)r);
+                sq += rp[c];
+                sk += rp[kDim + c];
+                sa += rp[2 * kDim + c];
+                sb += rp[3 * kDim];
+            }
+            const long long off = (row * H + h) * kDim + c;
+            float pre, a;
+            gate(p_x, expA, lb, pre, a);
+            const float dpre = pre >= lb ? sa * a : 0.f;
+            accA = fmaf(pre, dpre, accA);
+            const float dx = -expA * dpre / (1.f + expf(-p_x));
+            accB += dx;
+            P.dq[off] = sq;
+            P.dk[off] = sk;
+            P.dg[off] = dx;
+            if (rank == 0 && lane == 0) P.dbeta[row * H + h] = sb;
+        }
+        pend = false;
+    };
+
+    float C[4][4], Cn[4][4];  // checkpoint of the current segment, and of the next one
+    if (nseg > 0) {
+        fetch_segment(P, row0 + (long long)(nseg - 1) * kSeg, h, L - (nseg - 1) * kSeg, col0,
+                      true, tid, F);
+        load_piece(ckpt_at(nseg - 1), C, tid);
+    }
     for (int s = nseg - 1; s >= 0; --s) {
         const int len = min(kSeg, L - s * kSeg);
         const long long rs = row0 + (long long)s * kSeg;
         __syncthreads();
-        stage_segment(P, sm, rs, h, len, col0, expA, true, tid);
+        store_segment(sm, F, dtb, expA, lb, true, tid);
+        if (s > 0) {
+            fetch_segment(P, rs - kSeg, h, kSeg, col0, true, tid, F);
+            load_piece(ckpt_at(s - 1), Cn, tid);
+        }
         __syncthreads();
         for (int half = len > kHalf ? 1 : 0; half >= 0; --half) {
             const int t0 = half * kHalf, t1 = min(len, t0 + kHalf);
             {   // states entering tokens t0 .. t1 - 1, from the checkpoint
                 float R[4][4];
-                load_piece(ckpt_at(s), R, tid);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) R[i][m] = C[i][m];
                 for (int t = 0; t < t1; ++t) {
                     if (t >= t0) save_piece(st + (t - t0) * 4 * kThreads, R, tid);
                     if (t + 1 < t1) {
@@ -365,6 +482,8 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            const float x_here = t0 + warp < t1 ? xs[(t0 + warp) * kDim + rank * kVs + lane] : 0.f;
+            if (pend) finish_half();
             for (int t = t1 - 1; t >= t0; --t) {
                 float a[4], kk[4], qq[4], vv[4], oo[4], Sp[4][4];
                 ld4(as + t * kDim + 4 * lane, a);
@@ -374,65 +493,58 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
                 ld4(dos + t * kVs + 4 * warp, oo);
                 const float b = bs[t];
                 load_piece(st + (t - t0) * 4 * kThreads, Sp, tid);
-                // recompute: S~ = Diag(a) S, r = S~^T k, u = beta (v - r)
-                float St[4][4], r[4] = {0.f, 0.f, 0.f, 0.f};
+                // S~ = Diag(a) S and r = S~^T k; dS += scale q dO^T and du = dS^T k
+                // (one butterfly for both column sums)
+                float St[4][4], red[8];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int m = 0; m < 8; ++m) red[m] = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float sq = P.scale * qq[i];
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
                         St[i][m] = a[i] * Sp[i][m];
-                        r[m] = fmaf(St[i][m], kk[i], r[m]);
+                        red[m] = fmaf(St[i][m], kk[i], red[m]);
+                        dS[i][m] = fmaf(sq, oo[m], dS[i][m]);
+                        red[4 + m] = fmaf(dS[i][m], kk[i], red[4 + m]);
                     }
-                warp_sum4(r);
-                float e[4], u[4];
+                }
+                warp_sum8(red);
+                float e[4], u[4], du[4], dr[4], dbp = 0.f;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    e[m] = vv[m] - r[m];
+                    e[m] = vv[m] - red[m];
                     u[m] = b * e[m];
+                    du[m] = red[4 + m];
+                    dbp = fmaf(du[m], e[m], dbp);
+                    dr[m] = -b * du[m];
                 }
-                // o = scale S'^T q
-                float dqp[4], dkp[4], dap[4], du[4] = {0.f, 0.f, 0.f, 0.f};
+                float dqp[4], dkp[4], dap[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
+                    // o = scale S'^T q with S' = S~ + k u^T
                     float x = 0.f;
 #pragma unroll
                     for (int m = 0; m < 4; ++m) x = fmaf(fmaf(kk[i], u[m], St[i][m]), oo[m], x);
                     dqp[i] = P.scale * x;
-                    const float sq = P.scale * qq[i];
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        dS[i][m] = fmaf(sq, oo[m], dS[i][m]);
-                        du[m] = fmaf(dS[i][m], kk[i], du[m]);
-                    }
-                }
-                // S' = S~ + k u^T
-                warp_sum4(du);
-                float dbp = 0.f, dr[4];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    dbp = fmaf(du[m], e[m], dbp);
-                    dr[m] = -b * du[m];
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float x = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) x = fmaf(dS[i][m], u[m], x);
-                    // r = S~^T k
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        x = fmaf(St[i][m], dr[m], x);
-                        dS[i][m] = fmaf(kk[i], dr[m], dS[i][m]);
-                    }
-                    dkp[i] = x;
-                    // S~ = Diag(a) S
+                    // dk = dS u + S~ dr; then dS~ = dS + k dr^T
                     float y = 0.f;
 #pragma unroll
+                    for (int m = 0; m < 4; ++m) y = fmaf(dS[i][m], u[m], y);
+#pragma unroll
                     for (int m = 0; m < 4; ++m) {
-                        y = fmaf(dS[i][m], Sp[i][m], y);
+                        y = fmaf(St[i][m], dr[m], y);
+                        dS[i][m] = fmaf(kk[i], dr[m], dS[i][m]);
+                    }
+                    dkp[i] = y;
+                    // da = rowsum(dS~ o S); dS = Diag(a) dS~
+                    float z = 0.f;
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        z = fmaf(dS[i][m], Sp[i][m], z);
                         dS[i][m] *= a[i];
                     }
-                    dap[i] = y;
+                    dap[i] = z;
                 }
                 if (lane == 0) {
                     const float dvv[4] = {b * du[0], b * du[1], b * du[2], b * du[3]};
@@ -463,37 +575,23 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
                     dst[3 * kDim] = acc;
                 }
             }
-            // the pair's row sums over the four CTAs; then the per-channel outputs
-            cluster.sync();
-            if (t0 + warp < t1) {
-                const int c = rank * kVs + lane;
-                const long long row = rs + t0 + warp;
-                float sq = 0.f, sk = 0.f, sa = 0.f, sb = 0.f;
-#pragma unroll
-                for (int r = 0; r < kSlices; ++r) {
-                    const float* rp =
-                        cluster.map_shared_rank(part + (cb * kHalf + warp) * kPart, (unsigned)r);
-                    sq += rp[c];
-                    sk += rp[kDim + c];
-                    sa += rp[2 * kDim + c];
-                    sb += rp[3 * kDim];
-                }
-                const long long off = (row * H + h) * kDim + c;
-                const float x = __bfloat162float(P.g[off]) + P.dt_bias[(long long)h * kDim + c];
-                float pre, a;
-                gate(x, expA, lb, pre, a);
-                const float dpre = pre >= lb ? sa * a : 0.f;
-                accA = fmaf(pre, dpre, accA);
-                const float dx = -expA * dpre / (1.f + expf(-x));
-                accB += dx;
-                P.dq[off] = sq;
-                P.dk[off] = sk;
-                P.dg[off] = dx;
-                if (rank == 0 && lane == 0) P.dbeta[row * H + h] = sb;
-            }
+            // the CTA's row sums of this half are in part[cb]: publish them
+            cluster_arrive();
+            pend = true;
+            p_row = rs + t0;
+            p_len = t1 - t0;
+            p_cb = cb;
+            p_x = x_here;
             cb ^= 1;
         }
+        if (s > 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) C[i][m] = Cn[i][m];
+        }
     }
+    if (pend) finish_half();
 
     // 3. dS is now the gradient of the initial state
     if (P.dh0) {
