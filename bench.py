@@ -70,11 +70,19 @@ def counted_work(p):
     return head_tokens, flops, head_tokens * BYTES_PER_HEAD_TOKEN + state_bytes
 
 
+def l2_note(alg_bytes, what):
+    """How the timed steps stand to the 129 MB L2 (no explicit flush is made)."""
+    if alg_bytes > 129e6:
+        return "%s larger than L2 (%.2f GB per step vs 129 MB)" % (what, alg_bytes / 1e9)
+    return "%s fit in L2 (%.1f MB per step): cache-resident steps, no flush" % (
+        what, alg_bytes / 1e6)
+
+
 def workload_config(w, p, alg_bytes, head_tokens, flops, world):
     return {"workload": w.name, "B": p["B"], "T": p["T"], "H": p["H"], "K": D, "V": D,
             "seed": w.seed, "state_dtype": str(p["state_dtype"]).replace("torch.", ""),
             "parallelism": "replicas" if world > 1 else "single-gpu",
-            "l2": "inputs larger than L2 (%.2f GB per step vs 129 MB)" % (alg_bytes / 1e9),
+            "l2": l2_note(alg_bytes, "inputs"),
             "head_tokens_per_step": head_tokens, "counted_flop_per_step": flops,
             "counted_bytes_per_step": alg_bytes}
 
@@ -234,6 +242,202 @@ def job_throughput(units_per_rank, world, seconds):
     return units_per_rank * world / seconds
 
 
+# ----------------------------------------------------------------------------- backward pass
+
+METRIC_BWD = "KDA bwd head-tokens/s (all eight gradients, fp32)"
+# bytes per head-token the backward pass must move: q, k, v, g, dout (bf16) and beta
+# read; dq, dk, dv, dg (fp32) and dbeta written
+BWD_BYTES_PER_HEAD_TOKEN = 5 * 2 * D + 2 + 4 * 4 * D + 4
+# fp32 operations per head-token of one forward token step (decay, r = S~^T k,
+# rank-1 update: 3 D^2) and one reverse step (dq, dS += q dO^T, du, two for dk,
+# dS += k dr^T, da, dS *= a: 8 D^2), a fused multiply-add counting as one
+BWD_OPS_PER_HEAD_TOKEN = 11 * D * D
+# fp32 lanes x maximum SM clock: 152 SMs x 128 lanes x 2.07 GHz, in Gop/s
+FP32_LANE_PEAK_GOPS = 152 * 128 * 2.07
+
+
+def bwd_oracle_sample(p, ct, target_s, max_tokens=4096, fixed=None):
+    """Time the fp64 reverse-mode oracle (as it stands) on the first S tokens of every
+    head of the first sequence (it keeps every state of a pair, so S is capped)."""
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    H = p["H"]
+    L0 = seq_lengths(p)[0]
+
+    def run(S):
+        # sequence 0 starts at token 0 of batch row 0 (dense or packed)
+        S = max(1, min(S, L0))
+        sl = [x[:1, :S].contiguous() for x in (p["q"], p["k"], p["v"], p["g"], p["beta"])]
+        do = ct["dout"][:1, :S].contiguous()
+        h0 = None if p["initial_state"] is None else p["initial_state"][:1]
+        t0 = time.perf_counter()
+        oracle.recurrent_bwd(*sl, p["scale"], p["A_log"], p["dt_bias"], p["lower_bound"], do,
+                             initial_state=h0, dfinal_state=ct["dfinal_state"][:1],
+                             nthreads=cores)
+        return time.perf_counter() - t0, S
+
+    if fixed is not None:
+        dt, S = run(fixed)
+    else:
+        dt, S = run(256)
+        S2 = int(min(max_tokens, S * max(1.0, target_s / max(dt, 1e-3))))
+        if S2 > S:
+            dt, S = run(S2)
+    return {"value": S * H / dt, "unit": UNIT, "cores": min(cores, H), "kind": "oracle",
+            "tokens": S,
+            "sample": f"first {S} tokens of sequence 0 x {H} heads ({S * H} head-tokens), fp64 "
+                      f"reverse-mode C oracle, OpenMP over heads, {dt:.1f} s"}
+
+
+def bench_bwd(args, warmup, rank, world, local_rank, w):
+    """The backward pass (kda_bwd) on the workload: device-timed value, an end-to-end
+    figure through kda.bwd with pinned host buffers, and the oracle beside it."""
+    from gated_delta_rule_30_gb300 import inputs
+    p = inputs.make(w)
+    ct = inputs.cotangents(p, w.seed)
+    head_tokens = p["B"] * p["T"] * p["H"]
+    es = 0 if p["state_dtype"] is None else (4 if str(p["state_dtype"]) == "torch.float32" else 2)
+    state_bytes = p["N"] * p["H"] * D * D * (es + 4 + 4)  # h0 and dfinal read, dh0 written
+    alg_bytes = head_tokens * BWD_BYTES_PER_HEAD_TOKEN + state_bytes
+    ops = head_tokens * BWD_OPS_PER_HEAD_TOKEN
+    cfg = {"workload": w.name, "B": p["B"], "T": p["T"], "H": p["H"], "K": D, "V": D,
+           "seed": w.seed, "cotangent_seed": w.seed + 1000,
+           "state_dtype": str(p["state_dtype"]).replace("torch.", ""),
+           "parallelism": "replicas" if world > 1 else "single-gpu",
+           "l2": l2_note(alg_bytes, "inputs and gradients"),
+           "head_tokens_per_step": head_tokens, "counted_ops_per_step": ops,
+           "counted_bytes_per_step": alg_bytes}
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        res = bwd_oracle_sample(p, ct, target_s=2.0, max_tokens=1024)
+        rates = []
+        for i in range(warmup + args.steps):
+            r = bwd_oracle_sample(p, ct, 0.0, fixed=res["tokens"])
+            if i >= warmup:
+                rates.append(r["value"])
+        val = statistics.median(rates)
+        line = {"impl": "reference", "metric": METRIC_BWD, "value": val, "unit": UNIT,
+                "n_gpus": 1, "steps": args.steps, "warmup": warmup, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": cfg,
+                "cpu_baseline": {"value": val, "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                                 "sample": r["sample"]},
+                "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    import torch.distributed as dist
+
+    import gated_delta_rule_30_gb300 as kda
+    from gated_delta_rule_30_gb300 import build as kbuild
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    kbuild.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+    dout = ct["dout"].to(dev)
+    dhT = ct["dfinal_state"].to(dev)
+    ws = torch.empty(kda.bwd_workspace_size(p["B"], p["T"], p["H"],
+                                            p["N"] if p["cu_seqlens"] is not None else 0,
+                                            p["cu_seqlens"] is not None),
+                     dtype=torch.uint8, device=dev)
+
+    def step(x, dout_, dhT_):
+        return kda.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["A_log"],
+                       x["dt_bias"], x["lower_bound"], dout_, initial_state=x["initial_state"],
+                       dfinal_state=dhT_, cu_seqlens=x["cu_seqlens"], workspace=ws)
+
+    for _ in range(warmup):
+        step(d, dout, dhT)
+    torch.cuda.synchronize(dev)
+    kda.device_status(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(dev.index if world == 1 else local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step(d, dout, dhT)
+        ev[i + 1].record(stream)
+    barrier()
+    clk = clocks.stop()
+    kda.device_status(dev)
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    ms_step = max_over_ranks(ev[0].elapsed_time(ev[-1]) / args.steps, world, dev)
+
+    # end to end: pinned host inputs in, kda.bwd, every gradient back to pinned host memory
+    host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+    dout_h, dhT_h = ct["dout"].pin_memory(), ct["dfinal_state"].pin_memory()
+    in_keys = [k for k in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state",
+                           "cu_seqlens") if host.get(k) is not None]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in in_keys) + \
+        dout_h.numel() * 2 + dhT_h.numel() * 4
+    res = step(d, dout, dhT)
+    outs_h = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in res.items()
+              if v is not None}
+    d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
+    e2e_steps = max(1, args.e2e_steps)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for k in in_keys:
+            d[k].copy_(host[k], non_blocking=True)
+        dout.copy_(dout_h, non_blocking=True)
+        dhT.copy_(dhT_h, non_blocking=True)
+        res = step(d, dout, dhT)
+        for k, v in outs_h.items():
+            v.copy_(res[k], non_blocking=True)
+    e1.record(stream)
+    barrier()
+    kda.device_status(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+
+    ops_rate = ops / (ms_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC_BWD, "value": job_throughput(head_tokens, world, ms_step * 1e-3),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "alu", "kernel": "bwd", "achieved": ops_rate,
+                     "peak": FP32_LANE_PEAK_GOPS, "unit": "Gop/s",
+                     "frac": ops_rate / FP32_LANE_PEAK_GOPS, "traffic": None,
+                     "peak_kind": "derived: 152 SMs x 128 fp32 lanes x 2.07 GHz",
+                     "hbm_frac": alg_bytes / (ms_step * 1e-3) / 1e9 / peaks()[0],
+                     "note": "achieved = counted fp32 operations of one forward and one reverse "
+                             "token step per head-token / step time; the step is the backward "
+                             "kernel plus a 1-block parameter reduction"},
+        "step_ms_min_max": [min(per), max(per)],
+        "e2e": {"value": job_throughput(head_tokens, world, e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "note": "pinned host buffers, copies in, kda.bwd and copies out on one stream"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = bwd_oracle_sample(p, ct, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -246,6 +450,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
+                    help="fwd (default): the forward pass; bwd: its backward pass (kda_bwd)")
     ap.add_argument("--path", default="auto",
                     choices=["auto", "sliced", "transposed", "fused", "segmented"],
                     help="recurrence selection (default: the library's automatic choice)")
@@ -258,6 +464,8 @@ def main():
 
     from gated_delta_rule_30_gb300 import inputs
     w = inputs.WORKLOADS[args.workload]
+    if args.which == "bwd":
+        return bench_bwd(args, warmup, rank, world, local_rank, w)
 
     if args.impl == "reference":
         if rank != 0:
