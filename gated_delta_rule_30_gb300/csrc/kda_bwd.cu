@@ -28,11 +28,12 @@
 // are deterministic).
 //
 // Each CTA first runs the forward over the pair's tokens, storing its slice of
-// the state entering every 16-token segment (checkpoints, fp32, workspace).
-// It then takes the segments last to first: from the segment's checkpoint it
-// recomputes the states entering tokens 8..15 into shared memory, walks those
-// tokens backwards, then does the same for tokens 0..7.  Forward work per
-// token is thus 2.5 state updates; the backward walk is the rest.
+// the state entering tokens 0 and 8 of every 16-token segment (checkpoints,
+// fp32, workspace).  It then takes the segments last to first: from the
+// token-8 checkpoint it recomputes the states entering tokens 8..15 into
+// shared memory and walks those tokens backwards, then does the same for
+// tokens 0..7 from the token-0 checkpoint.  Forward work per token is thus
+// about 1.9 state updates; the backward walk is the rest.
 // This is the token-recurrent form of the backward pass, the plain GPU
 // counterpart of the fp64 reverse-mode oracle.
 #include <cooperative_groups.h>
@@ -101,11 +102,12 @@ struct BwdArgs {
     float* dh0;              // [N, H, K, V] fp32, or null
     float* part_dA;          // [N * H][kSlices]
     float* part_ddt;         // [N * H][K]
-    float* ckpt;             // [slots][H][kSlices][kSliceElems]
+    float* ckpt;             // [slots][H][kSlices][2][kSliceElems]
     int* status;
 };
 
-// Checkpoint slots of sequence n start at floor(cu[n] / 16) + n: consecutive
+// Checkpoint slots (two states each: entering tokens 0 and 8 of a 16-token
+// segment) of sequence n start at floor(cu[n] / 16) + n: consecutive
 // sequences' ranges cannot overlap (sequence n has at most floor(L / 16) + 1
 // segments), and all fit in floor(total / 16) + N + 1 slots.
 __host__ __device__ inline long long ckpt_slots(long long total, long long N) {
@@ -211,6 +213,57 @@ __device__ __forceinline__ void cluster_arrive() {
 }
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// Two forward tokens t and t + 1 with one column-sum butterfly.  The decayed
+// state of token t + 1 is a1 o (a0 o S + k0 u0^T), so
+//   r1 = (a1 o a0 o S)^T k1 + c u0,  c = sum_i a1_i k0_i k1_i:
+// both column sums and c come from the state before token t, and only the
+// scalar correction c u0 waits for u0.  Computes u0 and u1 and leaves
+// S = a0 o S (the decayed state of token t).
+__device__ __forceinline__ void pair_u(float (&S)[4][4], const float (&a0)[4], const float (&k0)[4],
+                                       const float (&v0)[4], float b0, const float (&a1)[4],
+                                       const float (&k1)[4], const float (&v1)[4], float b1,
+                                       float (&u0)[4], float (&u1)[4]) {
+    float p[8], ak1[4], c = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        ak1[i] = a1[i] * k1[i];
+        c = fmaf(ak1[i], k0[i], c);
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) p[m] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            S[i][m] *= a0[i];
+            p[m] = fmaf(S[i][m], k0[i], p[m]);
+            p[4 + m] = fmaf(S[i][m], ak1[i], p[4 + m]);
+        }
+    warp_sum8(p);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        u0[m] = b0 * (v0[m] - p[m]);
+        u1[m] = b1 * (v1[m] - p[4 + m] - c * u0[m]);
+    }
+}
+
+// S += k u^T, and S = a o S + k u^T.
+__device__ __forceinline__ void add_ku(float (&S)[4][4], const float (&kk)[4], const float (&u)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) S[i][m] = fmaf(kk[i], u[m], S[i][m]);
+}
+__device__ __forceinline__ void decay_add_ku(float (&S)[4][4], const float (&a)[4],
+                                             const float (&kk)[4], const float (&u)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) S[i][m] = fmaf(kk[i], u[m], a[i] * S[i][m]);
 }
 
 // One segment's token data as loaded from global memory (bf16 bit patterns),
@@ -381,30 +434,38 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
 
     const int nseg = (L + kSeg - 1) / kSeg;
     const long long slot0 = row0 / kSeg + n;
-    auto ckpt_at = [&](int s) {
-        return reinterpret_cast<float4*>(P.ckpt + (((slot0 + s) * H + h) * kSlices + rank) *
-                                                      (long long)kSliceElems);
+    // checkpoint of segment s: the state entering token 8 half of the segment
+    auto ckpt_at = [&](int s, int half) {
+        return reinterpret_cast<float4*>(
+            P.ckpt + ((((slot0 + s) * H + h) * kSlices + rank) * 2 + half) * (long long)kSliceElems);
     };
     Fetched F;
 
-    // 1. forward sweep: the state entering every segment (the last segment's
-    //    tokens are replayed by the walk, so the sweep stops before them);
-    //    the next segment's loads are in flight while a segment is swept
+    // 1. forward sweep: the states entering tokens 0 and 8 of every segment
+    //    (the last segment's tokens are replayed by the walk, so the sweep
+    //    stops before them); the next segment's loads are in flight while a
+    //    segment is swept.  Checkpoints are read back later by this same thread.
     if (nseg > 1) fetch_segment(P, row0, h, kSeg, col0, false, tid, F);
     for (int s = 0; s < nseg; ++s) {
-        save_piece(ckpt_at(s), S, tid);  // read back later by this same thread
+        save_piece(ckpt_at(s, 0), S, tid);
         if (s == nseg - 1) break;
         __syncthreads();
         store_segment(sm, F, dtb, expA, lb, false, tid);
         if (s + 2 < nseg)
             fetch_segment(P, row0 + (long long)(s + 1) * kSeg, h, kSeg, col0, false, tid, F);
         __syncthreads();
-        for (int t = 0; t < kSeg; ++t) {
-            float a[4], kk[4], vv[4];
-            ld4(as + t * kDim + 4 * lane, a);
-            ld4(ks + t * kDim + 4 * lane, kk);
-            ld4(vs + t * kVs + 4 * warp, vv);
-            fwd_token(S, a, kk, vv, bs[t]);
+        for (int t = 0; t < kSeg; t += 2) {
+            if (t == kHalf) save_piece(ckpt_at(s, 1), S, tid);
+            float a0[4], k0[4], v0[4], a1[4], k1[4], v1[4], u0[4], u1[4];
+            ld4(as + t * kDim + 4 * lane, a0);
+            ld4(ks + t * kDim + 4 * lane, k0);
+            ld4(vs + t * kVs + 4 * warp, v0);
+            ld4(as + (t + 1) * kDim + 4 * lane, a1);
+            ld4(ks + (t + 1) * kDim + 4 * lane, k1);
+            ld4(vs + (t + 1) * kVs + 4 * warp, v1);
+            pair_u(S, a0, k0, v0, bs[t], a1, k1, v1, bs[t + 1], u0, u1);
+            add_ku(S, k0, u0);
+            decay_add_ku(S, a1, k1, u1);
         }
     }
 
@@ -447,21 +508,21 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
         pend = false;
     };
 
-    float C[4][4], Cn[4][4];  // checkpoint of the current segment, and of the next one
+    // C: the checkpoint the current half is replayed from; Cn: the next half's.
+    // Halves are walked in the order (s, 1), (s, 0), (s - 1, 1), ...; the last
+    // segment has no token-8 checkpoint, so its upper half replays from token 0.
+    float C[4][4], Cn[4][4];
     if (nseg > 0) {
         fetch_segment(P, row0 + (long long)(nseg - 1) * kSeg, h, L - (nseg - 1) * kSeg, col0,
                       true, tid, F);
-        load_piece(ckpt_at(nseg - 1), C, tid);
+        load_piece(ckpt_at(nseg - 1, 0), C, tid);
     }
     for (int s = nseg - 1; s >= 0; --s) {
         const int len = min(kSeg, L - s * kSeg);
         const long long rs = row0 + (long long)s * kSeg;
         __syncthreads();
         store_segment(sm, F, dtb, expA, lb, true, tid);
-        if (s > 0) {
-            fetch_segment(P, rs - kSeg, h, kSeg, col0, true, tid, F);
-            load_piece(ckpt_at(s - 1), Cn, tid);
-        }
+        if (s > 0) fetch_segment(P, rs - kSeg, h, kSeg, col0, true, tid, F);
         __syncthreads();
         for (int half = len > kHalf ? 1 : 0; half >= 0; --half) {
             const int t0 = half * kHalf, t1 = min(len, t0 + kHalf);
@@ -471,14 +532,34 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
                     for (int m = 0; m < 4; ++m) R[i][m] = C[i][m];
-                for (int t = 0; t < t1; ++t) {
+                // the next half's checkpoint is loaded while this one is walked
+                if (half == 1) load_piece(ckpt_at(s, 0), Cn, tid);
+                else if (s > 0) load_piece(ckpt_at(s - 1, 1), Cn, tid);
+                // replay tokens tr .. t1 - 2, two at a time where possible
+                const int tr = (half == 1 && s < nseg - 1) ? kHalf : 0;
+                for (int t = tr; t < t1;) {
                     if (t >= t0) save_piece(st + (t - t0) * 4 * kThreads, R, tid);
-                    if (t + 1 < t1) {
+                    if (t + 1 >= t1) break;
+                    if (t + 2 < t1) {
+                        float a0[4], k0[4], v0[4], a1[4], k1[4], v1[4], u0[4], u1[4];
+                        ld4(as + t * kDim + 4 * lane, a0);
+                        ld4(ks + t * kDim + 4 * lane, k0);
+                        ld4(vs + t * kVs + 4 * warp, v0);
+                        ld4(as + (t + 1) * kDim + 4 * lane, a1);
+                        ld4(ks + (t + 1) * kDim + 4 * lane, k1);
+                        ld4(vs + (t + 1) * kVs + 4 * warp, v1);
+                        pair_u(R, a0, k0, v0, bs[t], a1, k1, v1, bs[t + 1], u0, u1);
+                        add_ku(R, k0, u0);
+                        if (t + 1 >= t0) save_piece(st + (t + 1 - t0) * 4 * kThreads, R, tid);
+                        decay_add_ku(R, a1, k1, u1);
+                        t += 2;
+                    } else {
                         float a[4], kk[4], vv[4];
                         ld4(as + t * kDim + 4 * lane, a);
                         ld4(ks + t * kDim + 4 * lane, kk);
                         ld4(vs + t * kVs + 4 * warp, vv);
                         fwd_token(R, a, kk, vv, bs[t]);
+                        t += 1;
                     }
                 }
             }
@@ -583,8 +664,6 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
             p_cb = cb;
             p_x = x_here;
             cb ^= 1;
-        }
-        if (s > 0) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -652,7 +731,7 @@ constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t ws_bytes(long long total, long long N, long long H) {
     const size_t pairs = (size_t)N * (size_t)H;
     return align256(pairs * kSlices * sizeof(float)) + align256(pairs * kDim * sizeof(float)) +
-           (size_t)ckpt_slots(total, N) * (size_t)H * kSlices * kSliceElems * sizeof(float);
+           (size_t)ckpt_slots(total, N) * (size_t)H * kSlices * 2 * kSliceElems * sizeof(float);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

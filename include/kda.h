@@ -1,5 +1,6 @@
 /*
- * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward pass.
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward pass and
+ * its backward pass (kda_bwd).
  *
  * The entry point mirrors the call printed in "Flashkda Delta Attention",
  * section "Core Kernel API":
@@ -202,8 +203,8 @@ size_t kda_noalloc_scratch_bytes(void);
  * 2-byte, dbeta: 4-byte); outputs must not overlap inputs or one another.
  * `workspace`: device memory of at least kda_bwd_workspace_size(...) bytes,
  * 256-byte aligned, or NULL to take it from the stream-ordered allocator on
- * `stream` (workspace_bytes is then ignored).  The scratch holds an fp32 copy
- * of the state entering every 16-token segment: about 4 KB per token per head.
+ * `stream` (workspace_bytes is then ignored).  The scratch holds fp32 copies
+ * of the state every 8 tokens: about 8 KB per token per head.
  * Asynchronous on `stream`; argument errors are reported synchronously and
  * launch nothing.  A malformed cu_seqlens (as for kda_fwd) is detected on the
  * device: the affected sequences are skipped and kda_device_status reports

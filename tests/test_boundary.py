@@ -210,12 +210,12 @@ def test_bwd_invalid_arguments_rejected(kda_lib, over):
 
 
 def test_bwd_workspace_size(kda_lib):
-    """Per-pair partial sums plus one fp32 state slice set (128 x 128) per head for
-    each of floor(total / 16) + N + 1 checkpoint slots."""
+    """Per-pair partial sums plus two fp32 states (128 x 128) per head for each of
+    floor(total / 16) + N + 1 checkpoint slots (states entering tokens 0 and 8)."""
     L = kda_lib.lib()
     n = L.kda_bwd_workspace_size(8, 2048, 16, 0, 0)
     slots = 8 * 2048 // 16 + 8 + 1
-    ckpt = slots * 16 * 128 * 128 * 4
+    ckpt = slots * 16 * 2 * 128 * 128 * 4
     assert ckpt <= n <= ckpt + 8 * 16 * (4 + 128) * 4 + 512
     assert L.kda_bwd_workspace_size(2, 64, 1, 3, 1) == 0
     assert L.kda_bwd_workspace_size(1, 100, 2, 3, 1) > 0
