@@ -170,3 +170,12 @@ def test_long_context_full_size_suffix(oracle_mod):
     part = {n: got[n].index_select(2, hs)[:, T - P:] for n in ("dq", "dk", "dv", "dg")}
     part["dbeta"] = got["dbeta"].index_select(2, hs)[:, T - P:]
     compare(part, ref, "long_context suffix", names=("dq", "dk", "dv", "dg", "dbeta"))
+
+
+@pytest.mark.parametrize("name", ["varlen_packed", "state_io"])
+def test_packed_workloads_full_size(oracle_mod, name):
+    """The full varlen_packed (32 sequences of 1..4096 tokens, H=32, bf16 state) and
+    state_io (1024 sequences of 1..128 tokens, H=32, fp32 state) workloads: every
+    element of all eight gradients of every (sequence, head) pair."""
+    w = inputs.WORKLOADS[name]
+    check(oracle_mod, inputs.make(w), w.seed, name)
