@@ -163,6 +163,16 @@ def l2norm(x, eps=L2NORM_EPS):
     return a
 
 
+def l2norm_bwd(x, dxhat, eps=L2NORM_EPS):
+    """Gradient with respect to x of sum(dxhat * l2norm(x)), row by row in float64:
+    with n = sqrt(sum x^2 + eps) and xhat = x / n, dx = (dxhat - xhat (xhat . dxhat)) / n."""
+    a = _f64(x)
+    d = np.asarray(dxhat, dtype=np.float64).reshape(a.shape)
+    n = np.sqrt(np.sum(a * a, axis=-1, keepdims=True) + eps)
+    xh = a / n
+    return (d - xh * np.sum(xh * d, axis=-1, keepdims=True)) / n
+
+
 def recurrent(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state=None,
               cu_seqlens=None, erase=1.0, nthreads=0, qk_l2norm=False):
     """Token-by-token recurrence (the definition).
@@ -226,7 +236,8 @@ def recurrent(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_stat
 
 
 def recurrent_bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout,
-                  initial_state=None, dfinal_state=None, cu_seqlens=None, nthreads=0):
+                  initial_state=None, dfinal_state=None, cu_seqlens=None, nthreads=0,
+                  qk_l2norm=False):
     """Reverse mode of ``recurrent`` (fp64): gradients of
     L = sum(dout * out) + sum(dfinal_state * final_state).
 
@@ -234,7 +245,20 @@ def recurrent_bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout,
     state [N, H, K, V] (None: no final-state term).  Returns a dict with dq, dk,
     dv, dg, dbeta (shaped like the inputs), dA_log [H], ddt_bias [H, K] and dh0
     [N, H, K, V], all float64.
+
+    qk_l2norm: the gradients of ``recurrent(..., qk_l2norm=True)``.  The
+    recurrence sees x_hat = x / n with n = sqrt(sum x^2 + eps) for every row of q
+    and k; by the chain rule through that map, dx = (dx_hat - x_hat (x_hat .
+    dx_hat)) / n, row by row (``l2norm_bwd``).
     """
+    if qk_l2norm:
+        qn, kn = l2norm(q), l2norm(k)
+        res = recurrent_bwd(qn, kn, v, g, beta, scale, A_log, dt_bias, lower_bound, dout,
+                            initial_state=initial_state, dfinal_state=dfinal_state,
+                            cu_seqlens=cu_seqlens, nthreads=nthreads)
+        res["dq"] = l2norm_bwd(q, res["dq"])
+        res["dk"] = l2norm_bwd(k, res["dk"])
+        return res
     B, T = _bt(q)
     cu = _cu(cu_seqlens, B, T)
     N = len(cu) - 1

@@ -120,3 +120,75 @@ def test_all_clamped_gate_has_no_gradient(oracle_mod):
     assert np.all(G["dg"] == 0.0) and np.all(G["ddt_bias"] == 0.0)
     assert np.all(G["dA_log"] == 0.0)
     assert np.abs(G["dq"]).max() > 0 and np.abs(G["dk"]).max() > 0
+
+
+def loss_qkn(oracle_mod, p, **over):
+    x = dict(p)
+    x.update(over)
+    out, hT = oracle_mod.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"],
+                                   x["A_log"], x["dt_bias"], x["lb"], initial_state=x["h0"],
+                                   cu_seqlens=x["cu"], qk_l2norm=True)
+    return float(np.sum(out * x["dout"]) + np.sum(hT * x["dhT"]))
+
+
+def test_qk_l2norm_directional_derivatives(oracle_mod):
+    """With the in-kernel q/k normalisation, <grad, D> equals the central difference
+    of the forward oracle run with qk_l2norm=True, for all eight inputs; q and k are
+    drawn with row norms far from 1, so the normalisation's Jacobian matters."""
+    rng = np.random.default_rng(RNG_SEED + 7)
+    p = problem(rng, [6, 0, 9], H=2, K=8, V=5, lower_bound=-3.0)
+    p["q"] = p["q"] * rng.uniform(0.2, 5.0, size=p["q"].shape[:-1] + (1,))
+    p["k"] = p["k"] * rng.uniform(0.2, 5.0, size=p["k"].shape[:-1] + (1,))
+    G = oracle_mod.recurrent_bwd(p["q"], p["k"], p["v"], p["g"], p["beta"], p["scale"],
+                                 p["A_log"], p["dt_bias"], p["lb"], p["dout"],
+                                 initial_state=p["h0"], dfinal_state=p["dhT"],
+                                 cu_seqlens=p["cu"], qk_l2norm=True)
+    for name, gname in NAMES.items():
+        D = rng.standard_normal(np.shape(p[name]))
+        eps = 1e-6
+        fd = (loss_qkn(oracle_mod, p, **{name: p[name] + eps * D})
+              - loss_qkn(oracle_mod, p, **{name: p[name] - eps * D})) / (2 * eps)
+        an = float(np.sum(G[gname] * D))
+        assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_l2norm_bwd_radial_component(oracle_mod):
+    """x / sqrt(|x|^2 + eps) changes along x only through eps: for any dxhat,
+    x . dx = (xhat . dxhat) eps / (|x|^2 + eps), and the tangential part of dx is
+    the tangential part of dxhat divided by n."""
+    rng = np.random.default_rng(RNG_SEED + 8)
+    x = rng.standard_normal((7, 3, 16)) * rng.uniform(0.01, 10.0, size=(7, 3, 1))
+    dxh = rng.standard_normal((7, 3, 16))
+    eps = oracle_mod.L2NORM_EPS
+    dx = oracle_mod.l2norm_bwd(x, dxh)
+    nn = np.sum(x * x, axis=-1)
+    n = np.sqrt(nn + eps)
+    xh = x / n[..., None]
+    np.testing.assert_allclose(np.sum(x * dx, axis=-1),
+                               np.sum(xh * dxh, axis=-1) * eps / (nn + eps), rtol=1e-9, atol=1e-15)
+    u = x / np.sqrt(nn)[..., None]
+    tan = lambda y: y - u * np.sum(u * y, axis=-1, keepdims=True)
+    np.testing.assert_allclose(tan(dx), tan(dxh) / n[..., None], rtol=1e-10, atol=1e-13)
+
+
+@pytest.mark.parametrize("mistake", ["radial term dropped", "not divided by n", "sign of the radial term"])
+def test_qk_l2norm_pin_catches_planted_mistakes(oracle_mod, monkeypatch, mistake):
+    """Each plausible slip in the normalisation's chain rule, planted in the oracle's
+    l2norm_bwd, makes the directional-derivative pin above fail."""
+    eps = oracle_mod.L2NORM_EPS
+
+    def wrong(x, dxhat, eps=eps):
+        a = np.asarray(x, dtype=np.float64)
+        d = np.asarray(dxhat, dtype=np.float64).reshape(a.shape)
+        n = np.sqrt(np.sum(a * a, axis=-1, keepdims=True) + eps)
+        xh = a / n
+        radial = xh * np.sum(xh * d, axis=-1, keepdims=True)
+        if mistake == "radial term dropped":
+            return d / n
+        if mistake == "not divided by n":
+            return d - radial
+        return (d + radial) / n
+
+    monkeypatch.setattr(oracle_mod, "l2norm_bwd", wrong)
+    with pytest.raises(AssertionError):
+        test_qk_l2norm_directional_derivatives(oracle_mod)
