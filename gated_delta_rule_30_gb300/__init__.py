@@ -85,7 +85,8 @@ def lib():
         L.kda_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         L.kda_bwd.restype = ctypes.c_int
         L.kda_bwd.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, f32, vp, ctypes.c_int, vp, vp, vp,
-                              i32, i32, i32, i32, i32, i32] + [vp] * 8 + [vp, ctypes.c_size_t, vp]
+                              i32, i32, i32, i32, i32, i32] + [vp] * 8 + \
+            [ctypes.c_uint32, vp, ctypes.c_size_t, vp]
         L.kda_bwd_workspace_size.restype = ctypes.c_size_t
         L.kda_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         L.kda_selftest_tcgen05.restype = ctypes.c_int
@@ -223,10 +224,31 @@ def chunk_kda(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale=None, initial
     With ``output_final_state`` a new final state [N, H, K, V] is returned, in the
     initial state's dtype (float32 when there is no initial state); otherwise
     ``final_state`` is None.  Everything else is as for ``fwd``.
+
+    Differentiable: when gradients are enabled and any of q, k, v, g, beta,
+    A_log, dt_bias or initial_state requires grad, the call is recorded for
+    autograd, and the backward pass is one ``kda_bwd`` call (see ``bwd``).  The
+    incoming gradient of ``o`` is used in bf16 (the kernel's dout dtype), that
+    of the final state in fp32; each returned gradient has its input's dtype.
     """
     import torch
     if scale is None:
         scale = q.shape[-1] ** -0.5
+    tensors = (q, k, v, g, beta, A_log, dt_bias, initial_state)
+    if torch.is_grad_enabled() and any(isinstance(t, torch.Tensor) and t.requires_grad
+                                       for t in tensors):
+        return _chunk_kda_function().apply(q, k, v, g, beta, A_log, dt_bias, initial_state,
+                                           cu_seqlens, float(lower_bound), float(scale),
+                                           bool(output_final_state),
+                                           bool(use_qk_l2norm_in_kernel))
+    return _chunk_kda_forward(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
+                              initial_state, output_final_state, cu_seqlens,
+                              use_qk_l2norm_in_kernel)
+
+
+def _chunk_kda_forward(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale, initial_state,
+                       output_final_state, cu_seqlens, use_qk_l2norm_in_kernel):
+    import torch
     o = torch.empty_like(v)
     hT = None
     if output_final_state:
@@ -238,6 +260,54 @@ def chunk_kda(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale=None, initial
     return o, hT
 
 
+_CHUNK_KDA_FN = None
+
+
+def _chunk_kda_function():
+    """The autograd Function behind a differentiable ``chunk_kda`` (made on first use,
+    so that importing this module does not import torch)."""
+    global _CHUNK_KDA_FN
+    if _CHUNK_KDA_FN is not None:
+        return _CHUNK_KDA_FN
+    import torch
+
+    class ChunkKDAFunction(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens, lower_bound,
+                    scale, output_final_state, qk_norm):
+            with torch.no_grad():
+                o, hT = _chunk_kda_forward(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
+                                           initial_state, output_final_state, cu_seqlens, qk_norm)
+            ctx.save_for_backward(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens)
+            ctx.cfg = (lower_bound, scale, qk_norm)
+            if hT is not None:
+                return o, hT
+            return o, None
+
+        @staticmethod
+        def backward(ctx, do, dhT):
+            q, k, v, g, beta, A_log, dt_bias, h0, cu = ctx.saved_tensors
+            lower_bound, scale, qk_norm = ctx.cfg
+            need = ctx.needs_input_grad
+            if do is None:
+                do = torch.zeros_like(v)
+            r = bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound,
+                    do.to(torch.bfloat16).contiguous(), initial_state=h0,
+                    dfinal_state=None if dhT is None else dhT.to(torch.float32).contiguous(),
+                    cu_seqlens=cu, want_dh0=h0 is not None and need[7],
+                    use_qk_l2norm_in_kernel=qk_norm)
+
+            def out(name, like, i):
+                return r[name].to(like.dtype) if need[i] else None
+
+            return (out("dq", q, 0), out("dk", k, 1), out("dv", v, 2), out("dg", g, 3),
+                    out("dbeta", beta, 4), out("dA_log", A_log, 5), out("ddt_bias", dt_bias, 6),
+                    None if h0 is None else out("dh0", h0, 7), None, None, None, None, None)
+
+    _CHUNK_KDA_FN = ChunkKDAFunction
+    return _CHUNK_KDA_FN
+
+
 def bwd_workspace_size(B: int, T: int, H: int, num_seqs: int = 0,
                        has_cu_seqlens: bool = False) -> int:
     n = lib().kda_bwd_workspace_size(B, T, H, num_seqs, 1 if has_cu_seqlens else 0)
@@ -247,14 +317,18 @@ def bwd_workspace_size(B: int, T: int, H: int, num_seqs: int = 0,
 
 
 def bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_state=None,
-        dfinal_state=None, cu_seqlens=None, workspace=None, want_dh0=True):
+        dfinal_state=None, cu_seqlens=None, workspace=None, want_dh0=True,
+        use_qk_l2norm_in_kernel=False):
     """Backward pass of ``fwd`` on the GPU (``kda_bwd``): gradients of
     L = sum(dout * out) + sum(dfinal_state * final_state).
 
     Inputs as for ``fwd``; ``dout``: bf16, shaped like ``v``; ``dfinal_state``:
     fp32 [N, H, 128, 128] or None.  Returns a dict of new fp32 tensors: dq, dk,
     dg (like q), dv (like v), dbeta (like beta), dA_log [H], ddt_bias [H, 128]
-    and dh0 [N, H, 128, 128] (None when ``want_dh0`` is false).  ``workspace``:
+    and dh0 [N, H, 128, 128] (None when ``want_dh0`` is false).
+    ``use_qk_l2norm_in_kernel``: the gradients of ``fwd`` with that flag (q and k
+    normalised row by row inside the kernels); dq and dk are then with respect to
+    the raw rows.  ``workspace``:
     optional uint8 device tensor of at least ``bwd_workspace_size`` bytes; by
     default the per-(device, stream) buffer that ``fwd`` also uses is grown and
     reused.
@@ -320,6 +394,7 @@ def bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_stat
                          _ptr(cu_seqlens), int(num_seqs), B, T, H, K, V,
                          *(_ptr(res[n]) for n in ("dq", "dk", "dv", "dg", "dbeta", "dA_log",
                                                   "ddt_bias", "dh0")),
+                         FWD_QK_L2NORM if use_qk_l2norm_in_kernel else 0,
                          ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(ws.numel()), stream))
     return res
 

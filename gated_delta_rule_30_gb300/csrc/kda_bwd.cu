@@ -92,6 +92,7 @@ struct BwdArgs {
     int h0_fp32;
     const float* dhT;        // [N, H, K, V] fp32, or null
     const int32_t* cu;       // [N + 1], or null (N sequences of T tokens)
+    int qk_norm;             // q and k rows used as x / sqrt(|x|^2 + eps)
     int N, H, T;
     long long total;         // tokens over all sequences
     float* dq;
@@ -304,7 +305,8 @@ __device__ __forceinline__ void fetch_segment(const BwdArgs& P, long long row0, 
 // CTA's columns, beta.  dtb: dt_bias of the thread's eight channels.
 // with_q: also q and dout.
 __device__ __forceinline__ void store_segment(uint8_t* sm, const Fetched& F, const float (&dtb)[8],
-                                              float expA, float lb, bool with_q, int tid) {
+                                              float expA, float lb, bool with_q, bool qk_norm,
+                                              int tid) {
     const int t = tid >> 4, c8 = (tid & 15) * 8;
     const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&F.k);
     const __nv_bfloat16* gb = reinterpret_cast<const __nv_bfloat16*>(&F.g);
@@ -317,6 +319,26 @@ __device__ __forceinline__ void store_segment(uint8_t* sm, const Fetched& F, con
         xx[e] = __bfloat162float(gb[e]) + dtb[e];
         float pre;
         gate(xx[e], expA, lb, pre, aa[e]);
+    }
+    if (qk_norm) {
+        // a token's 128 channels sit on the 16 lanes of one half-warp
+        float sk = 0.f, sq = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            sk = fmaf(kk[e], kk[e], sk);
+            sq = fmaf(qq[e], qq[e], sq);
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) {
+            sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        }
+        const float ik = 1.f / sqrtf(sk + kL2NormEps), iq = 1.f / sqrtf(sq + kL2NormEps);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            kk[e] *= ik;
+            qq[e] *= iq;
+        }
     }
     const int base = t * kDim + c8;
 #pragma unroll
@@ -450,7 +472,7 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
         save_piece(ckpt_at(s, 0), S, tid);
         if (s == nseg - 1) break;
         __syncthreads();
-        store_segment(sm, F, dtb, expA, lb, false, tid);
+        store_segment(sm, F, dtb, expA, lb, false, P.qk_norm != 0, tid);
         if (s + 2 < nseg)
             fetch_segment(P, row0 + (long long)(s + 1) * kSeg, h, kSeg, col0, false, tid, F);
         __syncthreads();
@@ -521,7 +543,7 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
         const int len = min(kSeg, L - s * kSeg);
         const long long rs = row0 + (long long)s * kSeg;
         __syncthreads();
-        store_segment(sm, F, dtb, expA, lb, true, tid);
+        store_segment(sm, F, dtb, expA, lb, true, P.qk_norm != 0, tid);
         if (s > 0) fetch_segment(P, rs - kSeg, h, kSeg, col0, true, tid, F);
         __syncthreads();
         for (int half = len > kHalf ? 1 : 0; half >= 0; --half) {
@@ -718,6 +740,45 @@ __global__ void bwd_param_kernel(const float* __restrict__ part_dA,
     }
 }
 
+// Chain rule through the q/k normalisation, in place: for every (token, head)
+// row of x (q or k, bf16) with n = sqrt(|x|^2 + eps) and xhat = x / n, the
+// gradient dxhat that the backward kernel wrote becomes
+// dx = (dxhat - xhat (xhat . dxhat)) / n.  One warp per row, four channels a lane.
+__global__ void __launch_bounds__(256) bwd_l2norm_kernel(const __nv_bfloat16* __restrict__ q,
+                                                         const __nv_bfloat16* __restrict__ k,
+                                                         float* __restrict__ dq,
+                                                         float* __restrict__ dk, long long rows) {
+    const long long row = blockIdx.x * 8ll + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const __nv_bfloat16* x = blockIdx.y == 0 ? q : k;
+    float* dx = blockIdx.y == 0 ? dq : dk;
+    const uint2 xr = *reinterpret_cast<const uint2*>(x + row * kDim + 4 * lane);
+    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&xr);
+    float xv[4], d[4];
+    ld4(dx + row * kDim + 4 * lane, d);
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        xv[e] = __bfloat162float(xb[e]);
+        ss = fmaf(xv[e], xv[e], ss);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = 1.f / sqrtf(ss + kL2NormEps);
+    float dot = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        xv[e] *= inv;
+        dot = fmaf(xv[e], d[e], dot);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) d[e] = (d[e] - xv[e] * dot) * inv;
+    st4(dx + row * kDim + 4 * lane, d);
+}
+
 }  // namespace bwd
 }  // namespace kda
 
@@ -761,10 +822,12 @@ extern "C" kda_status_t kda_bwd(const void* q, const void* k, const void* v, con
                                 const int32_t* cu_seqlens, int32_t num_seqs, int32_t B,
                                 int32_t T, int32_t H, int32_t K, int32_t V, float* dq, float* dk,
                                 float* dv, float* dg, float* dbeta, float* dA_log,
-                                float* ddt_bias, float* dinitial_state, void* workspace,
-                                size_t workspace_bytes_, void* stream) {
+                                float* ddt_bias, float* dinitial_state, uint32_t flags,
+                                void* workspace, size_t workspace_bytes_, void* stream) {
     using bwd::aligned16;
     clear_error();
+    if (flags & ~(uint32_t)KDA_FWD_QK_L2NORM)
+        return set_error(KDA_ERR_INVALID_ARGUMENT, "unknown flag bits");
     if (K != kDim || V != kDim)
         return set_error(KDA_ERR_INVALID_ARGUMENT, "K and V must both be 128");
     if (B < 1 || T < 0 || H < 1)
@@ -787,6 +850,8 @@ extern "C" kda_status_t kda_bwd(const void* q, const void* k, const void* v, con
     const long long N = cu_seqlens ? num_seqs : B;
     if ((long long)N * H * bwd::kSlices > (long long)INT32_MAX)
         return set_error(KDA_ERR_INVALID_ARGUMENT, "too many (sequence, head) pairs");
+    if ((total * H + 7) / 8 > (long long)INT32_MAX)
+        return set_error(KDA_ERR_INVALID_ARGUMENT, "too many (token, head) rows");
     if (total > 0) {
         if (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta)
             return set_error(KDA_ERR_INVALID_ARGUMENT,
@@ -845,6 +910,7 @@ extern "C" kda_status_t kda_bwd(const void* q, const void* k, const void* v, con
         a.h0_fp32 = initial_dtype == KDA_DTYPE_FP32;
         a.dhT = dfinal_state;
         a.cu = cu_seqlens;
+        a.qk_norm = (flags & KDA_FWD_QK_L2NORM) != 0;
         a.N = (int)N;
         a.H = H;
         a.T = T;
@@ -876,6 +942,13 @@ extern "C" kda_status_t kda_bwd(const void* q, const void* k, const void* v, con
                 static_cast<const uint8_t*>(ws) +
                 bwd::align256((size_t)N * H * bwd::kSlices * sizeof(float))),
             (int)N, H, dA_log, ddt_bias);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess && (flags & KDA_FWD_QK_L2NORM) && total > 0) {
+        const long long rows = total * H;  // (rows + 7) / 8 <= INT32_MAX, checked above
+        bwd::bwd_l2norm_kernel<<<dim3((unsigned)((rows + 7) / 8), 2), 256, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), dq, dk,
+            rows);
         e = cudaGetLastError();
     }
     kda_status_t rc = e == cudaSuccess ? KDA_OK : cuda_error(e, "backward kernel launch");

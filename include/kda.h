@@ -183,7 +183,8 @@ size_t kda_noalloc_scratch_bytes(void);
  * print the forward call only; the operation differentiated is the one stated
  * at the top of this file, q and k used as given).  Computes the gradients of
  *     L = sum(dout * out) + sum(dfinal_state * final_state)
- * with respect to every input:
+ * with respect to every input (q and k as given, or normalised first with
+ * KDA_FWD_QK_L2NORM in flags):
  *   dq, dk, dg     fp32 [B, T, H, K], written
  *   dv             fp32 [B, T, H, V], written
  *   dbeta          fp32 [B, T, H], written
@@ -194,6 +195,12 @@ size_t kda_noalloc_scratch_bytes(void);
  * v, g, beta, A_log, dt_bias, initial_state, cu_seqlens and the sizes) plus
  *   dout           bf16 [B, T, H, V], the gradient of out
  *   dfinal_state   fp32 [N, H, K, V], or NULL (no final-state term)
+ * flags: 0, or KDA_FWD_QK_L2NORM for the gradients of kda_fwd_ex with that
+ * flag: q and k enter the recurrence as x / sqrt(|x|^2 + 1e-6) row by row, and
+ * dq, dk are the gradients with respect to the raw rows (the chain rule through
+ * that map, dx = (dxhat - xhat (xhat . dxhat)) / n).  The normalised rows are
+ * used unrounded here (the forward rounds them to bf16; that rounding is taken
+ * as the identity).  Other bits return KDA_ERR_INVALID_ARGUMENT.
  * lower_bound: finite, <= 0 (no other range limit: the backward pass does not
  * use the forward's sub-block factorisation).  The clamp max(pre, lower_bound)
  * passes its gradient to the argument it returns, and to pre at a tie.
@@ -216,7 +223,7 @@ kda_status_t kda_bwd(const void* q, const void* k, const void* v, const void* g,
                      const void* dout, const float* dfinal_state, const int32_t* cu_seqlens,
                      int32_t num_seqs, int32_t B, int32_t T, int32_t H, int32_t K, int32_t V,
                      float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dA_log,
-                     float* ddt_bias, float* dinitial_state, void* workspace,
+                     float* ddt_bias, float* dinitial_state, uint32_t flags, void* workspace,
                      size_t workspace_bytes, void* stream);
 
 /* Bytes of device scratch kda_bwd needs for these sizes (does not read

@@ -184,13 +184,13 @@ def call_bwd(kda_lib, **over):
     a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=0.088, A_log=FAKE, dt_bias=FAKE,
              lb=-5.0, h0=None, h0d=0, dout=FAKE, dhT=None, cu=None, ns=0, B=1, T=64, H=2, K=128,
              V=128, dq=FAKE, dk=FAKE, dv=FAKE, dg=FAKE, dbeta=FAKE, dA=FAKE, ddt=FAKE, dh0=None,
-             ws=FAKE, wsb=0)
+             flags=0, ws=FAKE, wsb=0)
     a.update(over)
     L = kda_lib.lib()
     rc = L.kda_bwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["A_log"],
                    a["dt_bias"], a["lb"], a["h0"], a["h0d"], a["dout"], a["dhT"], a["cu"], a["ns"],
                    a["B"], a["T"], a["H"], a["K"], a["V"], a["dq"], a["dk"], a["dv"], a["dg"],
-                   a["dbeta"], a["dA"], a["ddt"], a["dh0"], a["ws"], a["wsb"], None)
+                   a["dbeta"], a["dA"], a["ddt"], a["dh0"], a["flags"], a["ws"], a["wsb"], None)
     return rc, L.kda_last_error_message().decode()
 
 
@@ -202,6 +202,7 @@ def call_bwd(kda_lib, **over):
     dict(dout=FAKE + 8), dict(dv=FAKE + 4), dict(dbeta=FAKE + 2), dict(dhT=FAKE + 8),
     dict(dh0=FAKE + 8), dict(cu=FAKE + 2, ns=1), dict(cu=FAKE, ns=-1),
     dict(wsb=1),                      # caller workspace smaller than kda_bwd_workspace_size
+    dict(flags=2), dict(flags=0x80000000),  # unknown flag bits
 ])
 def test_bwd_invalid_arguments_rejected(kda_lib, over):
     rc, msg = call_bwd(kda_lib, **over)

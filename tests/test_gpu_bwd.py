@@ -29,25 +29,25 @@ def custom(T=None, lens=None, H=2, state=torch.float32, seed=7, lower_bound=-5.0
     return inputs.make(w), seed
 
 
-def run_bwd(p, ct, with_dhT=True, workspace=None):
+def run_bwd(p, ct, with_dhT=True, workspace=None, qkn=False):
     import gated_delta_rule_30_gb300 as kda
     d = to_dev(p)
     dout = ct["dout"].cuda()
     dhT = ct["dfinal_state"].cuda() if with_dhT else None
     r = kda.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], d["A_log"], d["dt_bias"],
                 d["lower_bound"], dout, initial_state=d["initial_state"], dfinal_state=dhT,
-                cu_seqlens=d["cu_seqlens"], workspace=workspace)
+                cu_seqlens=d["cu_seqlens"], workspace=workspace, use_qk_l2norm_in_kernel=qkn)
     kda.device_status()
     torch.cuda.synchronize()
     return {n: r[n].cpu() for n in NAMES}
 
 
-def run_ref(oracle_mod, p, ct, with_dhT=True):
+def run_ref(oracle_mod, p, ct, with_dhT=True, qkn=False):
     return oracle_mod.recurrent_bwd(p["q"], p["k"], p["v"], p["g"], p["beta"], p["scale"],
                                     p["A_log"], p["dt_bias"], p["lower_bound"], ct["dout"],
                                     initial_state=p["initial_state"],
                                     dfinal_state=ct["dfinal_state"] if with_dhT else None,
-                                    cu_seqlens=p["cu_seqlens"])
+                                    cu_seqlens=p["cu_seqlens"], qk_l2norm=qkn)
 
 
 def compare(got, ref, what, names=NAMES):
@@ -60,10 +60,10 @@ def compare(got, ref, what, names=NAMES):
         assert mx <= RTOL * max(scale, 1e-30), f"{what} {n}: max_abs={mx:.3e}"
 
 
-def check(oracle_mod, p, seed, what, with_dhT=True):
+def check(oracle_mod, p, seed, what, with_dhT=True, qkn=False):
     ct = inputs.cotangents(p, seed)
-    got = run_bwd(p, ct, with_dhT)
-    ref = run_ref(oracle_mod, p, ct, with_dhT)
+    got = run_bwd(p, ct, with_dhT, qkn=qkn)
+    ref = run_ref(oracle_mod, p, ct, with_dhT, qkn=qkn)
     compare(got, ref, what)
     return got
 
@@ -179,3 +179,60 @@ def test_packed_workloads_full_size(oracle_mod, name):
     element of all eight gradients of every (sequence, head) pair."""
     w = inputs.WORKLOADS[name]
     check(oracle_mod, inputs.make(w), w.seed, name)
+
+
+@pytest.mark.parametrize("case", ["packed", "dense_no_state"])
+def test_qk_l2norm(oracle_mod, case):
+    """The gradients of the forward with in-kernel q/k normalisation: raw q and k rows
+    with norms spread over [0.05, 20] (the recipe of the forward's normalisation
+    tests), against the oracle's reverse mode through the normalisation."""
+    from test_gpu_qknorm import raw_qk
+    if case == "packed":
+        p, s = custom(lens=[70, 1, 129, 0, 33], H=2, seed=31)
+    else:
+        p, s = custom(T=100, B=2, H=3, state=None, seed=32)
+    check(oracle_mod, raw_qk(p, s), s, f"qk_l2norm {case}", qkn=True)
+
+
+def test_qk_l2norm_dense_prefill_full_size(oracle_mod):
+    """dense_prefill at full size with raw q and k normalised in the kernel: every
+    element of all eight gradients of all 128 pairs."""
+    from test_gpu_qknorm import raw_qk
+    w = inputs.WORKLOADS["dense_prefill"]
+    check(oracle_mod, raw_qk(inputs.make(w), w.seed), w.seed, "qk_l2norm dense_prefill", qkn=True)
+
+
+@pytest.mark.parametrize("qkn", [False, True])
+def test_autograd_chunk_kda(oracle_mod, qkn):
+    """chunk_kda is differentiable: loss.backward() through it gives, for every input,
+    the bf16/fp32 cast of kda.bwd's gradient bit for bit, and those gradients match
+    the oracle."""
+    import gated_delta_rule_30_gb300 as kda
+    from test_gpu_qknorm import raw_qk
+    p, s = custom(lens=[40, 17, 0, 66], H=2, seed=41)
+    if qkn:
+        p = raw_qk(p, s)
+    ct = inputs.cotangents(p, s)
+    d = to_dev(p)
+    names = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state")
+    leaf = {n: d[n].clone().requires_grad_(True) for n in names}
+    o, hT = kda.chunk_kda(leaf["q"], leaf["k"], leaf["v"], leaf["g"], leaf["beta"], leaf["A_log"],
+                          leaf["dt_bias"], p["lower_bound"], scale=p["scale"],
+                          initial_state=leaf["initial_state"], output_final_state=True,
+                          cu_seqlens=d["cu_seqlens"], use_qk_l2norm_in_kernel=qkn)
+    loss = (o.float() * ct["dout"].cuda().float()).sum() + (hT * ct["dfinal_state"].cuda()).sum()
+    loss.backward()
+    kda.device_status()
+    direct = run_bwd(p, ct, qkn=qkn)
+    grads = dict(zip(names, ("dq", "dk", "dv", "dg", "dbeta", "dA_log", "ddt_bias", "dh0")))
+    for n, gname in grads.items():
+        got = leaf[n].grad.cpu()
+        assert got.dtype == leaf[n].dtype, n
+        assert torch.equal(got, direct[gname].to(got.dtype)), n
+    ref = run_ref(oracle_mod, p, ct, qkn=qkn)
+    compare(direct, ref, f"autograd qkn={qkn}")
+    # without any input requiring grad, no graph is recorded
+    o2, _ = kda.chunk_kda(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"],
+                          p["lower_bound"], scale=p["scale"], initial_state=d["initial_state"],
+                          cu_seqlens=d["cu_seqlens"], use_qk_l2norm_in_kernel=qkn)
+    assert o2.grad_fn is None and torch.equal(o2, o.detach())
