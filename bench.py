@@ -14,6 +14,9 @@ independent replica of the workload (the pass has no cross-GPU exchange), so
 scaling is weak and value = all ranks' head-tokens / max-over-ranks time.
 ``--impl reference`` times the fp64 CPU oracle (the reference arm: there is
 no runnable reference implementation) on a bounded sample of the workload.
+``--pass bwd`` times the backward pass (``kda_bwd``: all eight gradients from
+resident inputs and output gradients) instead, with the same launch, JSON
+line and reference arm (the fp64 reverse-mode oracle).
 Prints one JSON line (rank 0).
 """
 from __future__ import annotations
