@@ -32,8 +32,11 @@
 // fp32, workspace).  It then takes the segments last to first: from the
 // token-8 checkpoint it recomputes the states entering tokens 8..15 into
 // shared memory and walks those tokens backwards, then does the same for
-// tokens 0..7 from the token-0 checkpoint.  Forward work per token is thus
-// about 1.9 state updates; the backward walk is the rest.
+// tokens 0..7 from the token-0 checkpoint.  Forward steps run two tokens per
+// column-sum butterfly (pair_u).  Forward work per token is thus about 1.9
+// state updates; the backward walk is the rest.
+// With the q/k normalisation flag the rows of q and k are staged normalised,
+// and a row kernel applies the normalisation's chain rule to dq and dk after.
 // This is the token-recurrent form of the backward pass, the plain GPU
 // counterpart of the fp64 reverse-mode oracle.
 #include <cooperative_groups.h>
