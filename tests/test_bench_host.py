@@ -46,3 +46,34 @@ def test_counted_work_single_token_step():
     assert head_tokens == 1024 * 32
     assert nbytes == 1024 * 32 * 1282 + 2 * 1024 * 32 * 128 * 128 * 4
     assert flops > 0
+
+
+def test_backward_reference_arm_line():
+    """bench.py --pass bwd --impl reference (the fp64 reverse-mode oracle on the host
+    cores) prints one JSON line with the contract's keys, on the small workload."""
+    import json
+    import subprocess
+    import sys
+    out = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--pass", "bwd",
+                          "--impl", "reference", "--workload", "ref_small", "--steps", "1",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=600,
+                         cwd=bench.ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [x for x in out.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC_BWD
+    assert line["value"] > 0 and line["unit"] == bench.UNIT and line["dtype"] == "f64"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["config"]["head_tokens_per_step"] == 512
+
+
+def test_backward_counted_work_constants():
+    """Counted bytes per head-token of the backward pass: q, k, v, g, dout (bf16)
+    and beta read, dq, dk, dv, dg (fp32) and dbeta written; counted operations:
+    11 D^2 (3 of a forward token step, 8 of a reverse one)."""
+    D = 128
+    assert bench.BWD_BYTES_PER_HEAD_TOKEN == 5 * 2 * D + 2 + 4 * 4 * D + 4
+    assert bench.BWD_OPS_PER_HEAD_TOKEN == 11 * D * D
+    assert abs(bench.FP32_LANE_PEAK_GOPS - 152 * 128 * 2.07) < 1e-9
