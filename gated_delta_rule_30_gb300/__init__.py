@@ -30,7 +30,8 @@ _LIB_PATH = os.path.join(_PKG, "libkda.so")
 _lib = None
 
 KDA_OK = 0
-FWD_QK_L2NORM = 1  # kda_fwd_ex flag
+FWD_QK_L2NORM = 1  # kda_fwd_ex flag (also a kda_bwd flag)
+BWD_LOW_MEMORY = 2  # kda_bwd flag
 _STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED",
            3: "KDA_ERR_CUDA", 4: "KDA_ERR_TIMEOUT", 5: "KDA_ERR_DEVICE_INPUT"}
 DTYPE_NONE, DTYPE_BF16, DTYPE_FP32 = 0, 1, 2
@@ -88,7 +89,7 @@ def lib():
                               i32, i32, i32, i32, i32, i32] + [vp] * 8 + \
             [ctypes.c_uint32, vp, ctypes.c_size_t, vp]
         L.kda_bwd_workspace_size.restype = ctypes.c_size_t
-        L.kda_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        L.kda_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32, ctypes.c_uint32]
         L.kda_selftest_tcgen05.restype = ctypes.c_int
         L.kda_selftest_tcgen05.argtypes = [vp, vp, vp, i32, i32, vp]
         _lib = L
@@ -309,8 +310,9 @@ def _chunk_kda_function():
 
 
 def bwd_workspace_size(B: int, T: int, H: int, num_seqs: int = 0,
-                       has_cu_seqlens: bool = False) -> int:
-    n = lib().kda_bwd_workspace_size(B, T, H, num_seqs, 1 if has_cu_seqlens else 0)
+                       has_cu_seqlens: bool = False, low_memory: bool = False) -> int:
+    n = lib().kda_bwd_workspace_size(B, T, H, num_seqs, 1 if has_cu_seqlens else 0,
+                                     BWD_LOW_MEMORY if low_memory else 0)
     if n == 0:
         _check(1)
     return int(n)
@@ -318,7 +320,7 @@ def bwd_workspace_size(B: int, T: int, H: int, num_seqs: int = 0,
 
 def bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_state=None,
         dfinal_state=None, cu_seqlens=None, workspace=None, want_dh0=True,
-        use_qk_l2norm_in_kernel=False):
+        use_qk_l2norm_in_kernel=False, low_memory=False):
     """Backward pass of ``fwd`` on the GPU (``kda_bwd``): gradients of
     L = sum(dout * out) + sum(dfinal_state * final_state).
 
@@ -328,7 +330,9 @@ def bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_stat
     and dh0 [N, H, 128, 128] (None when ``want_dh0`` is false).
     ``use_qk_l2norm_in_kernel``: the gradients of ``fwd`` with that flag (q and k
     normalised row by row inside the kernels); dq and dk are then with respect to
-    the raw rows.  ``workspace``:
+    the raw rows.  ``low_memory``: checkpoint the state every 64 tokens instead of
+    every 8 (about 1 KB of scratch per token per head instead of 8 KB; the same
+    results, bit for bit, and slower).  ``workspace``:
     optional uint8 device tensor of at least ``bwd_workspace_size`` bytes; by
     default the per-(device, stream) buffer that ``fwd`` also uses is grown and
     reused.
@@ -384,7 +388,10 @@ def bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_stat
            "dh0": torch.empty((N, H, K, V), dtype=f32, device=dev) if want_dh0 else None}
     stream = _stream_ptr(dev)
     with torch.cuda.device(dev):
-        need = L.kda_bwd_workspace_size(B, T, H, num_seqs, 1 if cu_seqlens is not None else 0)
+        flags = (FWD_QK_L2NORM if use_qk_l2norm_in_kernel else 0) | \
+            (BWD_LOW_MEMORY if low_memory else 0)
+        need = L.kda_bwd_workspace_size(B, T, H, num_seqs, 1 if cu_seqlens is not None else 0,
+                                        flags)
         if need == 0:
             _check(1)
         ws = workspace if workspace is not None else _workspace(dev, stream, need)
@@ -394,8 +401,8 @@ def bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_stat
                          _ptr(cu_seqlens), int(num_seqs), B, T, H, K, V,
                          *(_ptr(res[n]) for n in ("dq", "dk", "dv", "dg", "dbeta", "dA_log",
                                                   "ddt_bias", "dh0")),
-                         FWD_QK_L2NORM if use_qk_l2norm_in_kernel else 0,
-                         ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(ws.numel()), stream))
+                         flags, ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(ws.numel()),
+                         stream))
     return res
 
 

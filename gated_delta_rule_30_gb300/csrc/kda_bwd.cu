@@ -61,6 +61,8 @@ constexpr int kVs = kDim / kSlices;        // value columns per CTA (32)
 constexpr int kSeg = 16;                   // tokens per checkpoint segment
 constexpr int kHalf = 8;                   // tokens walked per recomputation
 constexpr int kSliceElems = kDim * kVs;    // 4096 floats per state slice
+constexpr int kChunkSegs = 4;              // segments per low-memory checkpoint (64 tokens)
+constexpr int kScratchSlots = 256;         // low-memory replay slots (>= CTAs resident at once)
 constexpr int kPart = 388;                 // dq[128] | dk[128] | da[128] | dbeta, padded
 
 // Dynamic shared memory of one CTA (byte offsets).
@@ -76,6 +78,9 @@ constexpr int kSmSlot = kSmB + kSeg * 4;                         // float [2][kW
 constexpr int kSmPart = kSmSlot + 2 * kWarps * kPart * 4;        // float [2][kHalf][kPart]
 constexpr int kSmemBytes = kSmPart + 2 * kHalf * kPart * 4;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory of the backward kernel");
+// more than half of an SM's 228 KB: one CTA per SM at a time, so fewer CTAs are
+// resident than there are low-memory replay slots (the launch checks the SM count)
+static_assert(2 * kSmemBytes > 228 * 1024, "the replay-slot pool assumes one CTA per SM");
 static_assert(kSmQ % 16 == 0 && kSmV % 16 == 0 && kSmDO % 16 == 0 && kSmSlot % 16 == 0 &&
                   kSmPart % 16 == 0 && (kPart * 4) % 16 == 0,
               "float4 areas must be 16-byte aligned");
@@ -106,7 +111,10 @@ struct BwdArgs {
     float* dh0;              // [N, H, K, V] fp32, or null
     float* part_dA;          // [N * H][kSlices]
     float* part_ddt;         // [N * H][K]
-    float* ckpt;             // [slots][H][kSlices][2][kSliceElems]
+    float* ckpt;             // [slots][H][kSlices][2][kSliceElems]; low-memory:
+                             // [slots64][H][kSlices][kSliceElems]
+    float* scratch;          // low-memory: [kScratchSlots][2 kChunkSegs][kSliceElems]
+    int* pool;               // low-memory: slot-in-use bitmap (kScratchSlots bits), zero at launch
     int* status;
 };
 
@@ -116,6 +124,10 @@ struct BwdArgs {
 // segments), and all fit in floor(total / 16) + N + 1 slots.
 __host__ __device__ inline long long ckpt_slots(long long total, long long N) {
     return total / kSeg + N + 1;
+}
+// Low-memory mode: one state per 64-token chunk, slots from floor(cu[n] / 64) + n.
+__host__ __device__ inline long long ckpt64_slots(long long total, long long N) {
+    return total / (kSeg * kChunkSegs) + N + 1;
 }
 
 __device__ __forceinline__ float softplus(float x) {
@@ -392,6 +404,9 @@ __device__ __forceinline__ void load_piece(const float4* base, float (&S)[4][4],
 // One cluster of kSlices CTAs per (sequence, head) pair; CTA rank r holds
 // value columns 32 r .. 32 r + 31 and writes dq, dk, dg of key channels
 // 32 r .. 32 r + 31.
+// kLowMem: checkpoints every 64 tokens, each chunk replayed into a scratch slot
+// (a template parameter, so the default kernel carries none of that code).
+template <bool kLowMem>
 __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
     bwd_kernel(const BwdArgs P) {
     extern __shared__ __align__(16) uint8_t sm[];
@@ -459,10 +474,55 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
 
     const int nseg = (L + kSeg - 1) / kSeg;
     const long long slot0 = row0 / kSeg + n;
+    const long long slot64 = row0 / (kSeg * kChunkSegs) + n;
+    // Low-memory mode: a replay slot for this CTA, claimed in the pool's
+    // occupancy bitmap (kScratchSlots bits in 32-bit words).  At most one CTA per
+    // SM is resident, so fewer than half the bits are ever set and every read of
+    // the bitmap shows free bits; a claim that loses a race retries with the
+    // word's newer value.  All loops are bounded.
+    __shared__ int s_scratch;
+    if (kLowMem) {
+        if (tid == 0) {
+            unsigned* bits = reinterpret_cast<unsigned*>(P.pool);
+            constexpr int kWords = kScratchSlots / 32;
+            int got = -1;
+            for (int pass = 0; pass < 64 && got < 0; ++pass) {
+                for (int w = 0; w < kWords && got < 0; ++w) {
+                    const int word = (int)((blockIdx.x + (unsigned)w) % kWords);
+                    unsigned cur = atomicOr(bits + word, 0u);
+                    for (int tries = 0; tries < 32 && cur != 0xffffffffu; ++tries) {
+                        const unsigned bit = 1u << (__ffs(~cur) - 1);
+                        const unsigned old = atomicOr(bits + word, bit);
+                        if (!(old & bit)) {
+                            got = word * 32 + __ffs(bit) - 1;
+                            break;
+                        }
+                        cur = old | bit;
+                    }
+                }
+            }
+            if (got < 0) {  // not reachable while fewer CTAs than slots are resident
+                atomicOr(P.status, kStatusLayout);
+                got = 0;
+            }
+            s_scratch = got;
+        }
+        __syncthreads();
+    }
     // checkpoint of segment s: the state entering token 8 half of the segment
+    // (low-memory: in this CTA's replay slot, by the segment's place in its chunk)
     auto ckpt_at = [&](int s, int half) {
+        if (kLowMem)
+            return reinterpret_cast<float4*>(
+                P.scratch + ((long long)s_scratch * 2 * kChunkSegs + (s % kChunkSegs) * 2 + half) *
+                                kSliceElems);
         return reinterpret_cast<float4*>(
             P.ckpt + ((((slot0 + s) * H + h) * kSlices + rank) * 2 + half) * (long long)kSliceElems);
+    };
+    // low-memory: the state entering 64-token chunk c
+    auto ckpt64_at = [&](int c) {
+        return reinterpret_cast<float4*>(
+            P.ckpt + (((slot64 + c) * H + h) * kSlices + rank) * (long long)kSliceElems);
     };
     Fetched F;
 
@@ -472,7 +532,8 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
     //    segment is swept.  Checkpoints are read back later by this same thread.
     if (nseg > 1) fetch_segment(P, row0, h, kSeg, col0, false, tid, F);
     for (int s = 0; s < nseg; ++s) {
-        save_piece(ckpt_at(s, 0), S, tid);
+        if (!kLowMem) save_piece(ckpt_at(s, 0), S, tid);
+        else if (s % kChunkSegs == 0) save_piece(ckpt64_at(s / kChunkSegs), S, tid);
         if (s == nseg - 1) break;
         __syncthreads();
         store_segment(sm, F, dtb, expA, lb, false, P.qk_norm != 0, tid);
@@ -480,7 +541,7 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
             fetch_segment(P, row0 + (long long)(s + 1) * kSeg, h, kSeg, col0, false, tid, F);
         __syncthreads();
         for (int t = 0; t < kSeg; t += 2) {
-            if (t == kHalf) save_piece(ckpt_at(s, 1), S, tid);
+            if (t == kHalf && !kLowMem) save_piece(ckpt_at(s, 1), S, tid);
             float a0[4], k0[4], v0[4], a1[4], k1[4], v1[4], u0[4], u1[4];
             ld4(as + t * kDim + 4 * lane, a0);
             ld4(ks + t * kDim + 4 * lane, k0);
@@ -540,11 +601,46 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
     if (nseg > 0) {
         fetch_segment(P, row0 + (long long)(nseg - 1) * kSeg, h, L - (nseg - 1) * kSeg, col0,
                       true, tid, F);
-        load_piece(ckpt_at(nseg - 1, 0), C, tid);
+        if (!kLowMem) load_piece(ckpt_at(nseg - 1, 0), C, tid);
     }
     for (int s = nseg - 1; s >= 0; --s) {
         const int len = min(kSeg, L - s * kSeg);
         const long long rs = row0 + (long long)s * kSeg;
+        if (kLowMem && (s == nseg - 1 || s % kChunkSegs == kChunkSegs - 1)) {
+            // entering 64-token chunk c from above: replay it from its checkpoint,
+            // writing the token-0 and token-8 states of its segments 4c .. s into
+            // the replay slot (the same operations as the sweep, so the same bits)
+            const int c = s / kChunkSegs;
+            float R[4][4];
+            Fetched G;
+            load_piece(ckpt64_at(c), R, tid);
+            for (int s2 = c * kChunkSegs; s2 <= s; ++s2) {
+                save_piece(ckpt_at(s2, 0), R, tid);
+                if (s2 == nseg - 1) break;  // the last segment is walked from its token 0
+                __syncthreads();
+                fetch_segment(P, row0 + (long long)s2 * kSeg, h, kSeg, col0, false, tid, G);
+                store_segment(sm, G, dtb, expA, lb, false, P.qk_norm != 0, tid);
+                __syncthreads();
+                const int tend = s2 == s ? kHalf : kSeg;  // segment s needs its token-8 state only
+                for (int t = 0; t < tend; t += 2) {
+                    if (t == kHalf) save_piece(ckpt_at(s2, 1), R, tid);
+                    float a0[4], k0[4], v0[4], a1[4], k1[4], v1[4], u0[4], u1[4];
+                    ld4(as + t * kDim + 4 * lane, a0);
+                    ld4(ks + t * kDim + 4 * lane, k0);
+                    ld4(vs + t * kVs + 4 * warp, v0);
+                    ld4(as + (t + 1) * kDim + 4 * lane, a1);
+                    ld4(ks + (t + 1) * kDim + 4 * lane, k1);
+                    ld4(vs + (t + 1) * kVs + 4 * warp, v1);
+                    pair_u(R, a0, k0, v0, bs[t], a1, k1, v1, bs[t + 1], u0, u1);
+                    add_ku(R, k0, u0);
+                    decay_add_ku(R, a1, k1, u1);
+                }
+                if (tend == kHalf) save_piece(ckpt_at(s2, 1), R, tid);
+            }
+            // the half walked first replays from this segment's token-8 state
+            // (token 0 for the last segment)
+            load_piece(ckpt_at(s, s < nseg - 1 ? 1 : 0), C, tid);
+        }
         __syncthreads();
         store_segment(sm, F, dtb, expA, lb, true, P.qk_norm != 0, tid);
         if (s > 0) fetch_segment(P, rs - kSeg, h, kSeg, col0, true, tid, F);
@@ -720,8 +816,12 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
         for (int w = 0; w < kWarps; ++w) x += slot[kThreads + w];
         P.part_dA[pair * kSlices + rank] = x;
     }
-    // no CTA leaves while a peer may still read its shared memory
+    // no CTA leaves while a peer may still read its shared memory; the replay
+    // slot goes back to the pool once every thread's scratch stores are visible
+    if (kLowMem) __threadfence();
     cluster.sync();
+    if (kLowMem && tid == 0)
+        atomicAnd(reinterpret_cast<unsigned*>(P.pool) + s_scratch / 32, ~(1u << (s_scratch % 32)));
 }
 
 // dA_log [H] and ddt_bias [H, K]: the per-pair sums added over the sequences
@@ -792,10 +892,16 @@ namespace {
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-size_t ws_bytes(long long total, long long N, long long H) {
+// Workspace: per-pair partial sums, then (low-memory) the slot pool and the
+// replay slots, then the checkpoints.
+size_t ws_bytes(long long total, long long N, long long H, bool low_mem) {
     const size_t pairs = (size_t)N * (size_t)H;
-    return align256(pairs * kSlices * sizeof(float)) + align256(pairs * kDim * sizeof(float)) +
-           (size_t)ckpt_slots(total, N) * (size_t)H * kSlices * 2 * kSliceElems * sizeof(float);
+    size_t b = align256(pairs * kSlices * sizeof(float)) + align256(pairs * kDim * sizeof(float));
+    if (low_mem)
+        return b + align256(kScratchSlots * sizeof(int)) +
+               (size_t)kScratchSlots * 2 * kChunkSegs * kSliceElems * sizeof(float) +
+               (size_t)ckpt64_slots(total, N) * (size_t)H * kSlices * kSliceElems * sizeof(float);
+    return b + (size_t)ckpt_slots(total, N) * (size_t)H * kSlices * 2 * kSliceElems * sizeof(float);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -807,14 +913,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 using namespace kda;
 
 extern "C" size_t kda_bwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t num_seqs,
-                                         int32_t has_cu_seqlens) {
+                                         int32_t has_cu_seqlens, uint32_t flags) {
     clear_error();
-    if (B < 1 || T < 0 || H < 1 || (has_cu_seqlens && (B != 1 || num_seqs < 0))) {
-        set_error(KDA_ERR_INVALID_ARGUMENT, "invalid sizes");
+    if (B < 1 || T < 0 || H < 1 || (has_cu_seqlens && (B != 1 || num_seqs < 0)) ||
+        (flags & ~(uint32_t)(KDA_FWD_QK_L2NORM | KDA_BWD_LOW_MEMORY))) {
+        set_error(KDA_ERR_INVALID_ARGUMENT, "invalid sizes or flags");
         return 0;
     }
     const long long N = has_cu_seqlens ? num_seqs : B;
-    return bwd::ws_bytes((long long)B * T, N, H);
+    return bwd::ws_bytes((long long)B * T, N, H, (flags & KDA_BWD_LOW_MEMORY) != 0);
 }
 
 extern "C" kda_status_t kda_bwd(const void* q, const void* k, const void* v, const void* g,
@@ -829,8 +936,9 @@ extern "C" kda_status_t kda_bwd(const void* q, const void* k, const void* v, con
                                 void* workspace, size_t workspace_bytes_, void* stream) {
     using bwd::aligned16;
     clear_error();
-    if (flags & ~(uint32_t)KDA_FWD_QK_L2NORM)
+    if (flags & ~(uint32_t)(KDA_FWD_QK_L2NORM | KDA_BWD_LOW_MEMORY))
         return set_error(KDA_ERR_INVALID_ARGUMENT, "unknown flag bits");
+    const bool low_mem = (flags & KDA_BWD_LOW_MEMORY) != 0;
     if (K != kDim || V != kDim)
         return set_error(KDA_ERR_INVALID_ARGUMENT, "K and V must both be 128");
     if (B < 1 || T < 0 || H < 1)
@@ -876,7 +984,7 @@ extern "C" kda_status_t kda_bwd(const void* q, const void* k, const void* v, con
     if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
         return set_error(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must be 4-byte aligned");
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const size_t need = bwd::ws_bytes(total, N, H);
+    const size_t need = bwd::ws_bytes(total, N, H, low_mem);
     void* ws = workspace;
     bool owned = false;
     if (N > 0) {
@@ -928,13 +1036,33 @@ extern "C" kda_status_t kda_bwd(const void* q, const void* k, const void* v, con
         p += bwd::align256(pairs * bwd::kSlices * sizeof(float));
         a.part_ddt = reinterpret_cast<float*>(p);
         p += bwd::align256(pairs * kDim * sizeof(float));
+        a.pool = nullptr;
+        a.scratch = nullptr;
+        if (low_mem) {
+            a.pool = reinterpret_cast<int*>(p);
+            p += bwd::align256(bwd::kScratchSlots * sizeof(int));
+            a.scratch = reinterpret_cast<float*>(p);
+            p += (size_t)bwd::kScratchSlots * 2 * bwd::kChunkSegs * bwd::kSliceElems * sizeof(float);
+        }
         a.ckpt = reinterpret_cast<float*>(p);
         a.status = status;
-        e = cudaFuncSetAttribute(bwd::bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        auto kernel = low_mem ? bwd::bwd_kernel<true> : bwd::bwd_kernel<false>;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  bwd::kSmemBytes);
+        // every replay slot free at launch; more slots than SMs
+        if (e == cudaSuccess && low_mem) {
+            int dev = 0, sms = 0;
+            e = cudaGetDevice(&dev);
+            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e == cudaSuccess && sms > bwd::kScratchSlots) {
+                if (owned) cudaFreeAsync(ws, st);
+                return set_error(KDA_ERR_UNSUPPORTED, "more SMs than low-memory replay slots");
+            }
+            if (e == cudaSuccess)
+                e = cudaMemsetAsync(a.pool, 0, bwd::kScratchSlots * sizeof(int), st);
+        }
         if (e == cudaSuccess) {
-            bwd::bwd_kernel<<<(unsigned)(pairs * bwd::kSlices), bwd::kThreads, bwd::kSmemBytes,
-                              st>>>(a);
+            kernel<<<(unsigned)(pairs * bwd::kSlices), bwd::kThreads, bwd::kSmemBytes, st>>>(a);
             e = cudaGetLastError();
         }
     }

@@ -195,12 +195,19 @@ size_t kda_noalloc_scratch_bytes(void);
  * v, g, beta, A_log, dt_bias, initial_state, cu_seqlens and the sizes) plus
  *   dout           bf16 [B, T, H, V], the gradient of out
  *   dfinal_state   fp32 [N, H, K, V], or NULL (no final-state term)
- * flags: 0, or KDA_FWD_QK_L2NORM for the gradients of kda_fwd_ex with that
- * flag: q and k enter the recurrence as x / sqrt(|x|^2 + 1e-6) row by row, and
- * dq, dk are the gradients with respect to the raw rows (the chain rule through
- * that map, dx = (dxhat - xhat (xhat . dxhat)) / n).  The normalised rows are
- * used unrounded here (the forward rounds them to bf16; that rounding is taken
- * as the identity).  Other bits return KDA_ERR_INVALID_ARGUMENT.
+ * flags: a combination of
+ *   KDA_FWD_QK_L2NORM   the gradients of kda_fwd_ex with that flag: q and k enter
+ *                       the recurrence as x / sqrt(|x|^2 + 1e-6) row by row, and
+ *                       dq, dk are the gradients with respect to the raw rows (the
+ *                       chain rule through that map, dx = (dxhat - xhat (xhat .
+ *                       dxhat)) / n).  The normalised rows are used unrounded
+ *                       here (the forward rounds them to bf16; that rounding is
+ *                       taken as the identity).
+ *   KDA_BWD_LOW_MEMORY  keep one fp32 state per 64 tokens (about 1 KB per token
+ *                       per head, plus 32 MiB) instead of one per 8 tokens (about
+ *                       8 KB); each 64-token chunk is replayed once more during
+ *                       the reverse walk.  Same results, bit for bit; slower.
+ * Other bits return KDA_ERR_INVALID_ARGUMENT.
  * lower_bound: finite, <= 0 (no other range limit: the backward pass does not
  * use the forward's sub-block factorisation).  The clamp max(pre, lower_bound)
  * passes its gradient to the argument it returns, and to pre at a tie.
@@ -211,7 +218,8 @@ size_t kda_noalloc_scratch_bytes(void);
  * `workspace`: device memory of at least kda_bwd_workspace_size(...) bytes,
  * 256-byte aligned, or NULL to take it from the stream-ordered allocator on
  * `stream` (workspace_bytes is then ignored).  The scratch holds fp32 copies
- * of the state every 8 tokens: about 8 KB per token per head.
+ * of the state every 8 tokens (about 8 KB per token per head), or every 64
+ * with KDA_BWD_LOW_MEMORY.
  * Asynchronous on `stream`; argument errors are reported synchronously and
  * launch nothing.  A malformed cu_seqlens (as for kda_fwd) is detected on the
  * device: the affected sequences are skipped and kda_device_status reports
@@ -226,10 +234,14 @@ kda_status_t kda_bwd(const void* q, const void* k, const void* v, const void* g,
                      float* ddt_bias, float* dinitial_state, uint32_t flags, void* workspace,
                      size_t workspace_bytes, void* stream);
 
-/* Bytes of device scratch kda_bwd needs for these sizes (does not read
- * cu_seqlens).  Returns 0 and sets the error message for invalid sizes. */
+/* kda_bwd flag: checkpoint the state every 64 tokens instead of every 8. */
+#define KDA_BWD_LOW_MEMORY 2u
+
+/* Bytes of device scratch kda_bwd needs for these sizes and flags (does not
+ * read cu_seqlens).  Returns 0 and sets the error message for invalid sizes or
+ * unknown flag bits. */
 size_t kda_bwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t num_seqs,
-                              int32_t has_cu_seqlens);
+                              int32_t has_cu_seqlens, uint32_t flags);
 
 /*
  * kda_device_status -- synchronises `stream`, then returns and clears the

@@ -214,9 +214,18 @@ def test_bwd_workspace_size(kda_lib):
     """Per-pair partial sums plus two fp32 states (128 x 128) per head for each of
     floor(total / 16) + N + 1 checkpoint slots (states entering tokens 0 and 8)."""
     L = kda_lib.lib()
-    n = L.kda_bwd_workspace_size(8, 2048, 16, 0, 0)
+    n = L.kda_bwd_workspace_size(8, 2048, 16, 0, 0, 0)
     slots = 8 * 2048 // 16 + 8 + 1
     ckpt = slots * 16 * 2 * 128 * 128 * 4
     assert ckpt <= n <= ckpt + 8 * 16 * (4 + 128) * 4 + 512
-    assert L.kda_bwd_workspace_size(2, 64, 1, 3, 1) == 0
-    assert L.kda_bwd_workspace_size(1, 100, 2, 3, 1) > 0
+    assert L.kda_bwd_workspace_size(2, 64, 1, 3, 1, 0) == 0
+    assert L.kda_bwd_workspace_size(1, 100, 2, 3, 1, 0) > 0
+    assert L.kda_bwd_workspace_size(1, 100, 2, 3, 1, 4) == 0   # unknown flag bit
+    # low memory: one state per 64 tokens, plus 256 replay slots of 8 states
+    lo = L.kda_bwd_workspace_size(8, 2048, 16, 0, 0, 2)
+    slots64 = 8 * 2048 // 64 + 8 + 1
+    ckpt64 = slots64 * 16 * 128 * 128 * 4
+    replay = 256 * 8 * 32 * 128 * 4
+    assert ckpt64 + replay <= lo <= ckpt64 + replay + 8 * 16 * (4 + 128) * 4 + 2048
+    long_ctx = L.kda_bwd_workspace_size(1, 65536, 32, 0, 0, 0)
+    assert L.kda_bwd_workspace_size(1, 65536, 32, 0, 0, 2) * 7 < long_ctx

@@ -29,14 +29,15 @@ def custom(T=None, lens=None, H=2, state=torch.float32, seed=7, lower_bound=-5.0
     return inputs.make(w), seed
 
 
-def run_bwd(p, ct, with_dhT=True, workspace=None, qkn=False):
+def run_bwd(p, ct, with_dhT=True, workspace=None, qkn=False, low_memory=False):
     import gated_delta_rule_30_gb300 as kda
     d = to_dev(p)
     dout = ct["dout"].cuda()
     dhT = ct["dfinal_state"].cuda() if with_dhT else None
     r = kda.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], d["A_log"], d["dt_bias"],
                 d["lower_bound"], dout, initial_state=d["initial_state"], dfinal_state=dhT,
-                cu_seqlens=d["cu_seqlens"], workspace=workspace, use_qk_l2norm_in_kernel=qkn)
+                cu_seqlens=d["cu_seqlens"], workspace=workspace, use_qk_l2norm_in_kernel=qkn,
+                low_memory=low_memory)
     kda.device_status()
     torch.cuda.synchronize()
     return {n: r[n].cpu() for n in NAMES}
@@ -236,3 +237,40 @@ def test_autograd_chunk_kda(oracle_mod, qkn):
                           p["lower_bound"], scale=p["scale"], initial_state=d["initial_state"],
                           cu_seqlens=d["cu_seqlens"], use_qk_l2norm_in_kernel=qkn)
     assert o2.grad_fn is None and torch.equal(o2, o.detach())
+
+
+@pytest.mark.parametrize("case", ["packed", "dense", "qk_l2norm"])
+def test_low_memory_bit_identical(oracle_mod, case):
+    """KDA_BWD_LOW_MEMORY keeps one state per 64 tokens and replays each chunk once
+    more: the same operations in the same order, so every gradient is bit-identical
+    to the default mode's.  Lengths sit on and around the 8-, 16- and 64-token
+    boundaries (0, 1, 8, 16, 17, 63, 64, 65, 100, 130, 192, 256, 257)."""
+    lens = [0, 1, 8, 16, 17, 63, 64, 65, 100, 130, 192, 256, 257]
+    if case == "dense":
+        p, s = custom(T=321, B=2, H=2, seed=51)
+    else:
+        p, s = custom(lens=lens, H=2, seed=52, state=torch.bfloat16)
+    qkn = case == "qk_l2norm"
+    if qkn:
+        from test_gpu_qknorm import raw_qk
+        p = raw_qk(p, s)
+    ct = inputs.cotangents(p, s)
+    a = run_bwd(p, ct, qkn=qkn)
+    b = run_bwd(p, ct, qkn=qkn, low_memory=True)
+    for n in NAMES:
+        assert torch.equal(a[n], b[n]), n
+    compare(b, run_ref(oracle_mod, p, ct, qkn=qkn), f"low memory {case}")
+
+
+@pytest.mark.parametrize("name", ["dense_prefill", "state_io"])
+def test_low_memory_full_size(name):
+    """Full workloads: low-memory gradients bit-identical to the default mode's
+    (which the full-size parity tests compare with the oracle).  state_io runs
+    131,072 short CTAs, so replay slots are claimed and returned at a high rate."""
+    w = inputs.WORKLOADS[name]
+    p = inputs.make(w)
+    ct = inputs.cotangents(p, w.seed)
+    a = run_bwd(p, ct)
+    b = run_bwd(p, ct, low_memory=True)
+    for n in NAMES:
+        assert torch.equal(a[n], b[n]), n
