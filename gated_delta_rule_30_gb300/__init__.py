@@ -218,7 +218,8 @@ def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state
 
 
 def chunk_kda(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale=None, initial_state=None,
-              output_final_state=False, cu_seqlens=None, use_qk_l2norm_in_kernel=False):
+              output_final_state=False, cu_seqlens=None, use_qk_l2norm_in_kernel=False,
+              low_memory_backward=False):
     """Allocating form of ``fwd``: returns ``(o, final_state)``.
 
     ``o`` is a new bf16 tensor shaped like ``v``.  ``scale`` defaults to K^-0.5.
@@ -231,6 +232,7 @@ def chunk_kda(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale=None, initial
     autograd, and the backward pass is one ``kda_bwd`` call (see ``bwd``).  The
     incoming gradient of ``o`` is used in bf16 (the kernel's dout dtype), that
     of the final state in fp32; each returned gradient has its input's dtype.
+    ``low_memory_backward``: run that backward pass with ``low_memory=True``.
     """
     import torch
     if scale is None:
@@ -241,7 +243,8 @@ def chunk_kda(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale=None, initial
         return _chunk_kda_function().apply(q, k, v, g, beta, A_log, dt_bias, initial_state,
                                            cu_seqlens, float(lower_bound), float(scale),
                                            bool(output_final_state),
-                                           bool(use_qk_l2norm_in_kernel))
+                                           bool(use_qk_l2norm_in_kernel),
+                                           bool(low_memory_backward))
     return _chunk_kda_forward(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
                               initial_state, output_final_state, cu_seqlens,
                               use_qk_l2norm_in_kernel)
@@ -275,12 +278,12 @@ def _chunk_kda_function():
     class ChunkKDAFunction(torch.autograd.Function):
         @staticmethod
         def forward(ctx, q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens, lower_bound,
-                    scale, output_final_state, qk_norm):
+                    scale, output_final_state, qk_norm, low_memory):
             with torch.no_grad():
                 o, hT = _chunk_kda_forward(q, k, v, g, beta, A_log, dt_bias, lower_bound, scale,
                                            initial_state, output_final_state, cu_seqlens, qk_norm)
             ctx.save_for_backward(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens)
-            ctx.cfg = (lower_bound, scale, qk_norm)
+            ctx.cfg = (lower_bound, scale, qk_norm, low_memory)
             if hT is not None:
                 return o, hT
             return o, None
@@ -288,7 +291,7 @@ def _chunk_kda_function():
         @staticmethod
         def backward(ctx, do, dhT):
             q, k, v, g, beta, A_log, dt_bias, h0, cu = ctx.saved_tensors
-            lower_bound, scale, qk_norm = ctx.cfg
+            lower_bound, scale, qk_norm, low_memory = ctx.cfg
             need = ctx.needs_input_grad
             if do is None:
                 do = torch.zeros_like(v)
@@ -296,14 +299,14 @@ def _chunk_kda_function():
                     do.to(torch.bfloat16).contiguous(), initial_state=h0,
                     dfinal_state=None if dhT is None else dhT.to(torch.float32).contiguous(),
                     cu_seqlens=cu, want_dh0=h0 is not None and need[7],
-                    use_qk_l2norm_in_kernel=qk_norm)
+                    use_qk_l2norm_in_kernel=qk_norm, low_memory=low_memory)
 
             def out(name, like, i):
                 return r[name].to(like.dtype) if need[i] else None
 
             return (out("dq", q, 0), out("dk", k, 1), out("dv", v, 2), out("dg", g, 3),
                     out("dbeta", beta, 4), out("dA_log", A_log, 5), out("ddt_bias", dt_bias, 6),
-                    None if h0 is None else out("dh0", h0, 7), None, None, None, None, None)
+                    None if h0 is None else out("dh0", h0, 7), None, None, None, None, None, None)
 
     _CHUNK_KDA_FN = ChunkKDAFunction
     return _CHUNK_KDA_FN

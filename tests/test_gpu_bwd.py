@@ -203,8 +203,8 @@ def test_qk_l2norm_dense_prefill_full_size(oracle_mod):
     check(oracle_mod, raw_qk(inputs.make(w), w.seed), w.seed, "qk_l2norm dense_prefill", qkn=True)
 
 
-@pytest.mark.parametrize("qkn", [False, True])
-def test_autograd_chunk_kda(oracle_mod, qkn):
+@pytest.mark.parametrize("qkn,low_memory", [(False, False), (True, False), (False, True)])
+def test_autograd_chunk_kda(oracle_mod, qkn, low_memory):
     """chunk_kda is differentiable: loss.backward() through it gives, for every input,
     the bf16/fp32 cast of kda.bwd's gradient bit for bit, and those gradients match
     the oracle."""
@@ -220,7 +220,8 @@ def test_autograd_chunk_kda(oracle_mod, qkn):
     o, hT = kda.chunk_kda(leaf["q"], leaf["k"], leaf["v"], leaf["g"], leaf["beta"], leaf["A_log"],
                           leaf["dt_bias"], p["lower_bound"], scale=p["scale"],
                           initial_state=leaf["initial_state"], output_final_state=True,
-                          cu_seqlens=d["cu_seqlens"], use_qk_l2norm_in_kernel=qkn)
+                          cu_seqlens=d["cu_seqlens"], use_qk_l2norm_in_kernel=qkn,
+                          low_memory_backward=low_memory)
     loss = (o.float() * ct["dout"].cuda().float()).sum() + (hT * ct["dfinal_state"].cuda()).sum()
     loss.backward()
     kda.device_status()
@@ -274,3 +275,35 @@ def test_low_memory_full_size(name):
     b = run_bwd(p, ct, low_memory=True)
     for n in NAMES:
         assert torch.equal(a[n], b[n]), n
+
+
+def test_caller_workspace_stream_and_no_dh0(oracle_mod):
+    """kda_bwd with an exactly sized caller workspace, on a side stream while the
+    default stream runs another backward pass, and without dinitial_state: the
+    gradients equal those of the plain call bit for bit."""
+    import gated_delta_rule_30_gb300 as kda
+    p, s = custom(lens=[90, 7, 33], H=2, seed=61)
+    ct = inputs.cotangents(p, s)
+    ref = run_bwd(p, ct)
+    d = to_dev(p)
+    need = kda.bwd_workspace_size(p["B"], p["T"], p["H"], p["N"], True)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    big, bs_ = custom(T=600, B=2, H=4, seed=62)
+    bct = inputs.cotangents(big, bs_)
+    bd = to_dev(big)
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    # the default stream's pass (own cached workspace) overlaps the side stream's
+    kda.bwd(bd["q"], bd["k"], bd["v"], bd["g"], bd["beta"], bd["scale"], bd["A_log"],
+            bd["dt_bias"], bd["lower_bound"], bct["dout"].cuda(),
+            initial_state=bd["initial_state"], dfinal_state=bct["dfinal_state"].cuda())
+    with torch.cuda.stream(side):
+        r = kda.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], d["A_log"],
+                    d["dt_bias"], d["lower_bound"], ct["dout"].cuda(side.device),
+                    initial_state=d["initial_state"], dfinal_state=ct["dfinal_state"].cuda(),
+                    cu_seqlens=d["cu_seqlens"], workspace=ws, want_dh0=False)
+    torch.cuda.synchronize()
+    kda.device_status()
+    assert r["dh0"] is None
+    for n in ("dq", "dk", "dv", "dg", "dbeta", "dA_log", "ddt_bias"):
+        assert torch.equal(r[n].cpu(), ref[n]), n
