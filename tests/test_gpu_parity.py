@@ -102,6 +102,15 @@ def test_chunk_records_match_oracle_stages(kda_lib, oracle_mod):
                 assert rel < 5e-3, f"{tag} {name}: rel_fro {rel:.3e}"
             np.testing.assert_allclose(d["gamma"], st["gamma"], rtol=1e-4, atol=1e-30,
                                        err_msg=tag)
+            # T = (I + A)^-1 itself, recovered from the record: U = T diag(beta) V and
+            # diag(beta) V (L x 128, random) has full row rank, so T = U pinv(diag(beta) V).
+            # U is bf16 in the record; the pseudo-inverse amplifies its rounding by the
+            # condition number of diag(beta) V (about 6 at L = 64): bound 2e-2, against
+            # an O(1) error for a wrong or transposed inverse.
+            T_gpu = d["U"][:L] @ np.linalg.pinv(b[:, None] * v)
+            rel, mx = errors(T_gpu, st["T"])
+            print(f"[stage] {tag} T: rel_fro={rel:.3e} max_abs={mx:.3e}")
+            assert rel < 2e-2, f"{tag} T: rel_fro {rel:.3e}"
             # padding rows/cols are exactly zero
             assert np.all(d["W"][L:] == 0) and np.all(d["Qhat"][L:] == 0)
             assert np.all(d["Ktil"][L:] == 0) and np.all(d["U"][L:] == 0)
