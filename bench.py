@@ -310,7 +310,7 @@ def bench_bwd(args, warmup, rank, world, local_rank, w):
            "parallelism": "replicas" if world > 1 else "single-gpu",
            "l2": l2_note(alg_bytes, "inputs and gradients"),
            "head_tokens_per_step": head_tokens, "counted_ops_per_step": ops,
-           "counted_bytes_per_step": alg_bytes}
+           "counted_bytes_per_step": alg_bytes, "low_memory": bool(args.low_memory)}
     if args.impl == "reference":
         if rank != 0:
             return 0
@@ -349,13 +349,16 @@ def bench_bwd(args, warmup, rank, world, local_rank, w):
     dhT = ct["dfinal_state"].to(dev)
     ws = torch.empty(kda.bwd_workspace_size(p["B"], p["T"], p["H"],
                                             p["N"] if p["cu_seqlens"] is not None else 0,
-                                            p["cu_seqlens"] is not None),
+                                            p["cu_seqlens"] is not None,
+                                            low_memory=args.low_memory),
                      dtype=torch.uint8, device=dev)
+    cfg["workspace_bytes"] = ws.numel()
 
     def step(x, dout_, dhT_):
         return kda.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["A_log"],
                        x["dt_bias"], x["lower_bound"], dout_, initial_state=x["initial_state"],
-                       dfinal_state=dhT_, cu_seqlens=x["cu_seqlens"], workspace=ws)
+                       dfinal_state=dhT_, cu_seqlens=x["cu_seqlens"], workspace=ws,
+                       low_memory=args.low_memory)
 
     for _ in range(warmup):
         step(d, dout, dhT)
@@ -455,6 +458,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
                     help="fwd (default): the forward pass; bwd: its backward pass (kda_bwd)")
+    ap.add_argument("--low-memory", action="store_true",
+                    help="with --pass bwd: the backward pass's low-memory mode (KDA_BWD_LOW_MEMORY)")
     ap.add_argument("--path", default="auto",
                     choices=["auto", "sliced", "transposed", "fused", "segmented"],
                     help="recurrence selection (default: the library's automatic choice)")
