@@ -985,23 +985,22 @@ extern "C" kda_status_t kda_bwd(const void* q, const void* k, const void* v, con
         return set_error(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must be 4-byte aligned");
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const size_t need = bwd::ws_bytes(total, N, H, low_mem);
+    if (N > 0 && workspace) {
+        if (workspace_bytes_ < need)
+            return set_error(KDA_ERR_INVALID_ARGUMENT,
+                             "workspace smaller than kda_bwd_workspace_size()");
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+            return set_error(KDA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+    }
+    int* status = device_status_ptr();  // before any allocation: nothing to undo on failure
+    if (!status) return KDA_ERR_CUDA;
     void* ws = workspace;
     bool owned = false;
-    if (N > 0) {
-        if (!ws) {
-            cudaError_t e = cudaMallocAsync(&ws, need, st);
-            if (e != cudaSuccess) return cuda_error(e, "cudaMallocAsync(workspace)");
-            owned = true;
-        } else {
-            if (workspace_bytes_ < need)
-                return set_error(KDA_ERR_INVALID_ARGUMENT,
-                                 "workspace smaller than kda_bwd_workspace_size()");
-            if (reinterpret_cast<uintptr_t>(ws) & 255u)
-                return set_error(KDA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
-        }
+    if (N > 0 && !ws) {
+        cudaError_t e = cudaMallocAsync(&ws, need, st);
+        if (e != cudaSuccess) return cuda_error(e, "cudaMallocAsync(workspace)");
+        owned = true;
     }
-    int* status = device_status_ptr();
-    if (!status) return KDA_ERR_CUDA;
     cudaError_t e = cudaSuccess;
     if (N > 0) {
         const size_t pairs = (size_t)N * (size_t)H;

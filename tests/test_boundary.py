@@ -202,7 +202,8 @@ def call_bwd(kda_lib, **over):
     dict(dout=FAKE + 8), dict(dv=FAKE + 4), dict(dbeta=FAKE + 2), dict(dhT=FAKE + 8),
     dict(dh0=FAKE + 8), dict(cu=FAKE + 2, ns=1), dict(cu=FAKE, ns=-1),
     dict(wsb=1),                      # caller workspace smaller than kda_bwd_workspace_size
-    dict(flags=2), dict(flags=0x80000000),  # unknown flag bits
+    dict(flags=4), dict(flags=0x80000000),  # unknown flag bits
+    dict(flags=2),                    # low memory: the workspace (0 bytes) is too small
 ])
 def test_bwd_invalid_arguments_rejected(kda_lib, over):
     rc, msg = call_bwd(kda_lib, **over)
