@@ -481,6 +481,8 @@ extern "C" kda_status_t kda_device_status(void* stream) {
     if (e != cudaSuccess) return cuda_error(e, "clear status");
     if (host & kStatusLayout)
         return set_error(KDA_ERR_CUDA, "a kernel's shared-memory area was not 1024-byte aligned");
+    if (host & kStatusScratch)
+        return set_error(KDA_ERR_CUDA, "the backward pass found no free low-memory replay slot");
     if (host & kStatusTimeout) return set_error(KDA_ERR_TIMEOUT, "a bounded device wait timed out");
     if (host & kStatusDeviceInput)
         return set_error(KDA_ERR_DEVICE_INPUT, "malformed cu_seqlens detected on the device");

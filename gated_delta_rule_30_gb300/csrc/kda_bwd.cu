@@ -502,7 +502,7 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
             if (got < 0) {  // not reachable while fewer CTAs than slots are resident
-                atomicOr(P.status, kStatusLayout);
+                atomicOr(P.status, kStatusScratch);
                 got = 0;
             }
             s_scratch = got;

@@ -249,7 +249,9 @@ size_t kda_bwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t num_seqs,
  * cu_seqlens seen by an earlier call), KDA_ERR_TIMEOUT (a bounded
  * device-side wait gave up; that call's outputs are undefined) or KDA_ERR_CUDA
  * (a chunk kernel found its shared-memory area misaligned for its swizzled
- * tensor store and skipped its work; outputs undefined).
+ * tensor store and skipped its work, or a low-memory kda_bwd call found no free
+ * replay slot, which cannot happen while at most one of its CTAs runs per SM;
+ * outputs undefined).
  */
 kda_status_t kda_device_status(void* stream);
 
