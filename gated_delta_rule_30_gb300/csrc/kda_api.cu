@@ -12,6 +12,7 @@
 
 #include "kda.h"
 #include "kda_internal.h"
+#include "kda_bwd_status.h"
 
 namespace kda {
 

@@ -48,6 +48,7 @@
 
 #include "kda.h"
 #include "kda_internal.h"
+#include "kda_bwd_status.h"
 
 namespace kda {
 namespace bwd {

@@ -115,7 +115,6 @@ int* device_status_ptr();
 constexpr int kStatusDeviceInput = 1;
 constexpr int kStatusTimeout = 2;
 constexpr int kStatusLayout = 4;  // a kernel found its shared-memory area misaligned (skipped its work)
-constexpr int kStatusScratch = 8;  // the backward pass found no free replay slot (outputs undefined)
 
 // Kernel launchers (kda_prep.cu, kda_recur.cu, kda_recur_t.cu, kda_api.cu).
 cudaError_t launch_schedule(const Problem& p, const Workspace& ws, int* status, cudaStream_t st);
