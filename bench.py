@@ -100,6 +100,7 @@ KERNEL_SOURCES = {
     "recurrence/segmented": ("kda_recur.cu",),
     "maps": ("kda_recur.cu", "kda_segmented.cu"),
     "scan": ("kda_segmented.cu",),
+    "bwd": ("kda_bwd.cu", "kda_bwd_status.h"),
 }
 # kernels one forward pass launches, per path
 LAUNCHES = {"sliced": 3, "transposed": 3, "fused": 2, "decode": 1, "segmented": 6}
@@ -451,6 +452,14 @@ def bench_bwd(args, warmup, rank, world, local_rank, w):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
 
     ops_rate = ops / (ms_step * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath) and not args.low_memory:
+        with open(tpath) as f:
+            tr = json.load(f).get("bwd", {})
+        if tr.get("source_sha256_16") == kernel_source_hash("bwd") and \
+                tr.get("workload") == args.workload:
+            traffic = tr.get("bytes_per_launch")
     line = {
         "metric": METRIC_BWD, "value": job_throughput(head_tokens, world, ms_step * 1e-3),
         "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": warmup,
@@ -458,7 +467,7 @@ def bench_bwd(args, warmup, rank, world, local_rank, w):
         "dtype": "f32", "data": "synthetic", "config": cfg,
         "roofline": {"bound": "alu", "kernel": "bwd", "achieved": ops_rate,
                      "peak": FP32_LANE_PEAK_GOPS, "unit": "Gop/s",
-                     "frac": ops_rate / FP32_LANE_PEAK_GOPS, "traffic": None,
+                     "frac": ops_rate / FP32_LANE_PEAK_GOPS, "traffic": traffic,
                      "peak_kind": "derived: 152 SMs x 128 fp32 lanes x 2.07 GHz",
                      "hbm_frac": alg_bytes / (ms_step * 1e-3) / 1e9 / peaks()[0],
                      "note": "achieved = counted fp32 operations of one forward and one reverse "
