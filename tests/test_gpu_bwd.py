@@ -307,3 +307,18 @@ def test_caller_workspace_stream_and_no_dh0(oracle_mod):
     assert r["dh0"] is None
     for n in ("dq", "dk", "dv", "dg", "dbeta", "dA_log", "ddt_bias"):
         assert torch.equal(r[n].cpu(), ref[n]), n
+
+
+def test_no_sequences():
+    """cu_seqlens = [0] (no sequences, no tokens): nothing is walked; dA_log and
+    ddt_bias are written as zeros and the state gradient is empty."""
+    import gated_delta_rule_30_gb300 as kda
+    p, s = custom(lens=[], H=3, seed=71, state=None)
+    assert p["N"] == 0 and p["T"] == 0
+    d = to_dev(p)
+    ct = inputs.cotangents(p, s)
+    r = kda.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], d["A_log"], d["dt_bias"],
+                d["lower_bound"], ct["dout"].cuda(), cu_seqlens=d["cu_seqlens"])
+    kda.device_status()
+    assert torch.count_nonzero(r["dA_log"]) == 0 and torch.count_nonzero(r["ddt_bias"]) == 0
+    assert r["dh0"].shape == (0, 3, 128, 128) and r["dq"].numel() == 0
