@@ -78,6 +78,11 @@ WORKLOADS["long_context_8k"] = Workload("long_context_8k: B=1 T=8192 H=32, fp32 
 # smaller decoding step used for profiler captures (states still exceed L2: 2 x 0.5 GB)
 WORKLOADS["decode_256"] = Workload("decode_256: B=256 T=1 H=32, fp32 state", 256, 1, 32, 5,
                                    state_dtype=torch.float32)
+# smaller instance of state_io used for profiler captures (256 sequences; states and inputs
+# still exceed L2: 1 GB of fp32 states in and out)
+WORKLOADS["state_io_256"] = Workload("state_io_256: 256 seqs U[1,128] H=32, fp32 state", 1, None,
+                                     32, 4, n_seqs=256, len_range=(1, 128),
+                                     state_dtype=torch.float32)
 WORKLOAD_ORDER = ["ref_small", "dense_prefill", "varlen_packed", "long_context", "state_io"]
 
 
