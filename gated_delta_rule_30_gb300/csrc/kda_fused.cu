@@ -99,6 +99,7 @@ cudaError_t launch_fused(const Problem& p, const Workspace& ws, int* status, cud
     if (e != cudaSuccess) return e;
     FusedArgs a;
     if (!prep::make_prep_args(p, ws, status, a.p)) return cudaErrorInvalidValue;
+    a.p.hint_records = 1;  // the recurrence reads each record back within a few chunks
     a.r = recur_t::make_recur_t_args(p, ws, status);
     a.ready = ws.ready;
     a.n_rec = p.N * p.H;

@@ -104,6 +104,7 @@ struct PrepArgs {
     int H;
     int N;
     int qk_norm;  // normalise each q and k row (token) to unit L2 norm first
+    int hint_records;  // store records with an L2 evict_last policy (read back soon, fused launch)
     const int32_t* flags;
     const int32_t* chunk_off;
     const ChunkInfo* info;
@@ -114,16 +115,20 @@ struct PrepArgs {
 __device__ __forceinline__ float lds_bf16(const uint8_t* base, uint32_t off) {
     return bf16_to_f(*reinterpret_cast<const uint16_t*>(base + off));
 }
-__device__ __forceinline__ void stg_v4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+// 16-byte record store with the L2 policy `pol` (see l2_policy_evict_last)
+__device__ __forceinline__ void stg_v4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                       uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(a),
+                 "r"(b), "r"(c), "r"(d), "l"(pol)
+                 : "memory");
 }
 __device__ __forceinline__ void sts_v4f(uint32_t saddr, const float (&x)[8]) {
     st_shared_v4(saddr, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
                  pack_bf16(x[6], x[7]));
 }
-__device__ __forceinline__ void stg_v4f(uint8_t* p, const float (&x)[8]) {
+__device__ __forceinline__ void stg_v4f(uint8_t* p, const float (&x)[8], uint64_t pol) {
     stg_v4(p, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-           pack_bf16(x[6], x[7]));
+           pack_bf16(x[6], x[7]), pol);
 }
 
 // Factors of the right score operands, produced eight tokens at a time (the
@@ -210,21 +215,22 @@ __device__ __forceinline__ void sub_sync(uint32_t bar_id) {
 }
 // One TMA tile copy (box of the tensor map at coordinates {x, y, z}) into shared
 // memory, completing on `bar`.
+// The inputs are read once: the copies mark their lines evict_first in L2.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
-                                            uint64_t* bar) {
+                                            uint64_t* bar, uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-        "%3, %4}], [%5];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(pol)
         : "memory");
 }
 // TMA tensor store of one box from shared memory, in the thread's bulk async-group.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z,
-                                             const void* src) {
+                                             const void* src, uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], "
+        "[%4], %5;" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(smem_addr(src)), "l"(pol)
         : "memory");
 }
 // Row `ch` (64 bf16 values, 128 B) of a 128 x 64 tile in the 128-byte swizzled
@@ -360,6 +366,10 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
                                           const bool relinquish) {
 
     if (P.flags[0] != 1) return;
+    // L2 policies: the inputs are streamed once; the records are read back soon
+    // by the fused launch's recurrence (elsewhere they outgrow L2: no hint)
+    const uint64_t pol_in = l2_policy_evict_first();
+    const uint64_t pol_rec = P.hint_records ? l2_policy_evict_last() : l2_policy_evict_normal();
     // a CTA that already gave up on a bounded wait poisons the launch: skip the
     // rest (decided once, so every thread of the worker takes the same path)
     if (tid == 0) {
@@ -390,14 +400,14 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     // next sequence's tokens) are zeroed after landing.
     auto stage_g = [&](int tok0, int hh) {  // thread 0
         mbar_arrive_expect_tx(&S.bar_g, kChunk * kDim * 2);
-        tma_load_3d(sm + kSmG, &P.tm_g, 0, hh, tok0, &S.bar_g);
+        tma_load_3d(sm + kSmG, &P.tm_g, 0, hh, tok0, &S.bar_g, pol_in);
     };
     auto stage_qkv = [&](int tok0, int hh, float beta_t) {
         if (tid == 0) {
             mbar_arrive_expect_tx(&S.bar_qkv, 3 * kChunk * kDim * 2);
-            tma_load_3d(sm + kSmQ, &P.tm_q, 0, hh, tok0, &S.bar_qkv);
-            tma_load_3d(sm + kSmK, &P.tm_k, 0, hh, tok0, &S.bar_qkv);
-            tma_load_3d(sm + kSmV, &P.tm_v, 0, hh, tok0, &S.bar_qkv);
+            tma_load_3d(sm + kSmQ, &P.tm_q, 0, hh, tok0, &S.bar_qkv, pol_in);
+            tma_load_3d(sm + kSmK, &P.tm_k, 0, hh, tok0, &S.bar_qkv, pol_in);
+            tma_load_3d(sm + kSmV, &P.tm_v, 0, hh, tok0, &S.bar_qkv, pol_in);
         }
         if (tid < kChunk) S.sBeta[tid] = beta_t;
     };
@@ -558,7 +568,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
                 qh[u] = P.scale * QV(uu) * E;
             }
             sts_v4f(smem_addr(sm + kSmKbT + kmaj_off(ch, t0 + tg * 8, 128, 1024)), kb);
-            stg_v4f(rec + kRecWQ + mnmaj_off(64 + t0 + tg * 8, ch, 128, 2048), qh);
+            stg_v4f(rec + kRecWQ + mnmaj_off(64 + t0 + tg * 8, ch, 128, 2048), qh, pol_rec);
         }
         if (half == 0) reinterpret_cast<float*>(rec + kRecGam)[ch] = P0 * P1;
         // suffix pass: (K o F)^T to the record
@@ -572,7 +582,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
                 kt[u] = KV(uu) * F;
                 F *= al[uu];
             }
-            stg_v4f(rec + kRecKT + kmaj_off(ch, t0 + tg * 8, 128, 1024), kt);
+            stg_v4f(rec + kRecKT + kmaj_off(ch, t0 + tg * 8, 128, 1024), kt, pol_rec);
         }
     }
     sub_sync(bar_id);  // staging fully consumed; Left / R may now overwrite it
@@ -743,8 +753,8 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
                         hi[u] = __bfloat162float(__float2bfloat16_rn(val[8 * hh + u]));
                         lo[u] = val[8 * hh + u] - hi[u];
                     }
-                    stg_v4f(rec + kRecAQ + kmaj_off(i, jb + 8 * hh, 128, 1024), hi);
-                    stg_v4f(rec + kRecAQL + kmaj_off(i, jb + 8 * hh, 128, 1024), lo);
+                    stg_v4f(rec + kRecAQ + kmaj_off(i, jb + 8 * hh, 128, 1024), hi, pol_rec);
+                    stg_v4f(rec + kRecAQL + kmaj_off(i, jb + 8 * hh, 128, 1024), lo, pol_rec);
                 }
             }
         }
@@ -755,8 +765,8 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
 #pragma unroll
                 for (int jg = 0; jg < 2; ++jg) {
                     const int j0 = 32 + 16 * hj + 8 * jg;
-                    stg_v4(rec + kRecAQ + kmaj_off(i, j0, 128, 1024), 0u, 0u, 0u, 0u);
-                    stg_v4(rec + kRecAQL + kmaj_off(i, j0, 128, 1024), 0u, 0u, 0u, 0u);
+                    stg_v4(rec + kRecAQ + kmaj_off(i, j0, 128, 1024), 0u, 0u, 0u, 0u, pol_rec);
+                    stg_v4(rec + kRecAQL + kmaj_off(i, j0, 128, 1024), 0u, 0u, 0u, 0u, pol_rec);
                 }
             }
             // zero the strictly upper 16 x 16 blocks of T (q-row warps, while the
@@ -903,7 +913,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
                     float x[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) x[u] = __uint_as_float(r[c][8 * hh + u]);
-                    stg_v4f(rec + kRecWQ + mnmaj_off(16 * c + 8 * hh, ch, 128, 2048), x);
+                    stg_v4f(rec + kRecWQ + mnmaj_off(16 * c + 8 * hh, ch, 128, 2048), x, pol_rec);
                 }
             }
         } else {
@@ -915,7 +925,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& P, uint8_t* sm, PrepSh
     // tensor store and the flag release
     sub_sync(bar_id);
     if (tid == kStoreTid) {
-        tma_store_3d(&P.tm_ut, 0, 0, chunk * H + h, sm + kSmKbT);
+        tma_store_3d(&P.tm_ut, 0, 0, chunk * H + h, sm + kSmKbT, pol_rec);
         bulk_commit();
         // the flag follows once the store has completed (next item's read-out, or
         // the exit)
@@ -1008,6 +1018,7 @@ inline bool make_prep_args(const Problem& p, const Workspace& ws, int* status, P
     a.H = p.H;
     a.N = p.N;
     a.qk_norm = p.qk_norm ? 1 : 0;
+    a.hint_records = 0;
     a.flags = ws.flags;
     a.chunk_off = ws.chunk_off;
     a.info = ws.info;

@@ -379,6 +379,8 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
             // ---------------------------------------------------- producer
             if (lane == 0) {
                 int fillsA[kStages] = {0, 0}, fillsB[kStages] = {0, 0};
+                // a record is dead once copied: its lines may leave L2 first
+                const uint64_t pol_rec = l2_policy_evict_first();
                 constexpr int kAhead = kStages + 2;  // records pulled into L2 ahead
                 if (!ready)
                     for (int i = 0; i < kAhead && i < nchunks; ++i)
@@ -406,14 +408,14 @@ __device__ __forceinline__ void recur_t_body(const RecurTArgs& P, uint8_t* sm, R
                         fence_async_global();
                     }
                     mbar_arrive_expect_tx(&S.full[s], kPartA0Bytes + kPartA1Bytes);
-                    bulk_g2s(dst + kPartA0, rec + kPartA0, kPartA0Bytes, &S.full[s]);
-                    bulk_g2s(dst + kPartA1, rec + kPartA1, kPartA1Bytes, &S.full[s]);
+                    bulk_g2s_hint(dst + kPartA0, rec + kPartA0, kPartA0Bytes, &S.full[s], pol_rec);
+                    bulk_g2s_hint(dst + kPartA1, rec + kPartA1, kPartA1Bytes, &S.full[s], pol_rec);
                     ++fillsA[s];
                     // part B once that chunk's MMAs are done
                     if (fillsB[s] > 0) WAIT_OR_ABORT(&S.empty[s], (uint32_t)((fillsB[s] - 1) & 1));
                     if (*((volatile int*)&S.s_abort)) break;
                     mbar_arrive_expect_tx(&S.fullB[s], kPartBBytes);
-                    bulk_g2s(dst + kPartB, rec + kPartB, kPartBBytes, &S.fullB[s]);
+                    bulk_g2s_hint(dst + kPartB, rec + kPartB, kPartBBytes, &S.fullB[s], pol_rec);
                     ++fillsB[s];
                 }
                 // drain: every issued fill must have landed before the CTA exits
