@@ -106,11 +106,15 @@ KERNEL_SOURCES = {
 LAUNCHES = {"sliced": 3, "transposed": 3, "fused": 2, "decode": 1, "segmented": 6}
 
 
+# shared headers each kernel's sources include (the forward kernels all include tc.cuh)
+SHARED_HEADERS = {"bwd": ("kda_internal.h",)}
+
+
 def kernel_source_hash(kernel):
     """Hash of a kernel's sources and the headers they include, with comments and
     whitespace removed (a comment edit does not make stored counters stale)."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES[kernel] + ("tc.cuh", "kda_internal.h"):
+    for name in KERNEL_SOURCES[kernel] + SHARED_HEADERS.get(kernel, ("tc.cuh", "kda_internal.h")):
         with open(os.path.join(ROOT, "gated_delta_rule_30_gb300", "csrc", name)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
